@@ -1,0 +1,300 @@
+"""Plain CPU oracle for the AWQ W4A16 group-quantized linear layer.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py`` may import this module.  The
+product library never calls it, and this module imports nothing from the
+product package: the two sides share only the seeded input generator in
+``awq_inputs``.
+
+Sources (web pages describing Activation-aware Weight Quantization):
+
+* [P1] "awq-quantization（AWQ量化技术）Skill 是什么？如何下载安装使用？"
+  (skillsbot.cn), sections "该技能的主要功能和特点" and "步骤 2/3".
+* [P2] "AWQ量化实战：无需重训，把大模型压进4bit显存" (xdnf.cn), §1.1, §2.1-§2.3,
+  §3.3, §3.4, §5.1.
+* [P4] "大模型量化部署实战：GPTQ与AWQ算法" (yunthe.com), section
+  "大模型量化的核心原理与位宽选择".
+* [P5] "什么是激活感知权重量化（AWQ）？" (aiboss88.com), section "工作机制".
+
+Everything is written for clarity, not speed: fp32 where the method's
+integer decisions are taken (so that a code is decided exactly as the
+definition says), fp64 for every sum.  Readings taken where the pages are
+silent are marked READING.
+
+Parity status: every function here is pinned by a ``-m "not gpu"`` test
+against closed forms, invariants, brute force on tiny inputs or hand-derived
+golden values (tests/test_oracle_pins.py).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 128          # [P1] 步骤 2 quant_config q_group_size; [P2] §2.3
+W_BIT = 4            # [P1] 步骤 2 w_bit
+QMAX = (1 << W_BIT) - 1
+N_GRID = 20          # number of alpha candidates, all in [0, 1)
+A_FLOOR = np.float32(1e-8)          # READING: floor on mean|x| before the power
+S_MIN = np.float32(2.0 ** -14)      # READING: smallest normal fp16 step
+S_MAX = np.float32(65504.0)         # READING: largest finite fp16 step
+TOL_REL = 4e-3       # per-element matmul tolerance (relative to sum |x~ w^|)
+MSE_REL = 1e-4       # search tolerance on the MSE of the chosen alpha
+
+
+# ---------------------------------------------------------------- a1: stats
+def absmean(X16: np.ndarray) -> np.ndarray:
+    """Per-input-channel activation strength ``a_c = mean_t |x_tc|``.
+
+    [P2] §2.1: collect the calibration activations of every input channel,
+    take absolute values and average over many tokens (a running mean or a
+    plain sum-then-divide are both acceptable).  READING: plain mean, summed
+    in fp64, stored as fp32.
+    """
+    X = np.asarray(X16)
+    T = X.shape[0]
+    acc = np.zeros(X.shape[1], dtype=np.float64)
+    for t0 in range(0, T, 4096):                # bounded memory only
+        acc += np.abs(X[t0:t0 + 4096].astype(np.float64)).sum(axis=0)
+    return (acc / T).astype(np.float32)
+
+
+# ------------------------------------------------------- a2: scale candidates
+def alpha_grid(n_grid: int = N_GRID) -> np.ndarray:
+    """The alpha candidates ``{0, 1/n, ..., (n-1)/n}`` (fp64).
+
+    [P2] §2.2: the scale is found by a grid search over a candidate interval.
+    READING: 20 evenly spaced points in [0, 1), starting at 0.
+    """
+    return np.arange(n_grid, dtype=np.float64) / n_grid
+
+
+def channel_scales(a: np.ndarray, alpha: float):
+    """Activation-aware per-channel scales ``s_c = a_c ** alpha`` and ``1/s_c``.
+
+    [P2] §2.2 and [P5] 工作机制: salient channels (large mean|x|) are scaled
+    up by a factor derived from the offline activation statistics.
+    READING: ``a`` is floored at 1e-8 (fp32) so that 1/s_c stays finite; the
+    power is taken in fp64 and rounded to fp32; no normalisation of s_c.
+    ``inv_s`` is the IEEE fp32 quotient ``1 / s_c``.
+    """
+    a32 = np.maximum(np.asarray(a, dtype=np.float32), A_FLOOR)
+    s_c = np.power(a32.astype(np.float64), float(alpha)).astype(np.float32)
+    inv_s = (np.float32(1.0) / s_c).astype(np.float32)
+    return s_c, inv_s
+
+
+# --------------------------------------------------- a3: scaled group RTN
+def quantize(W16: np.ndarray, s_c: np.ndarray | None = None):
+    """Asymmetric group round-to-nearest of ``W' = W diag(s_c)``.
+
+    [P2] §1.1 (round to nearest), §2.1 (the channel is the input dimension;
+    the weight is out x in and is grouped along the input dimension), §2.3
+    (128 consecutive input channels share one step), [P4] (a scale plus a
+    zero point per group), [P1] 步骤 2 (zero_point on, 4 bits, group 128).
+
+    For each row n and group g of 128 input channels (fp32 arithmetic):
+      mn, mx = min, max of the group of w'                 (READING: plain)
+      s32    = (mx - mn) / 15, clamped to [2^-14, 65504]   (READING)
+      s      = fp16_rne(s32)            (the stored scale; codes use it)
+      z      = clamp(rint(-mn / s), 0, 15)
+      q      = clamp(rint(w' / s) + z, 0, 15)
+    with ``rint`` = round half to even and IEEE fp32 division.
+
+    Returns ``q`` uint8 [N, K], ``z`` uint8 [N, G], ``s16`` float16 [N, G].
+    """
+    W = np.asarray(W16, dtype=np.float16).astype(np.float32)
+    N, K = W.shape
+    assert K % GROUP == 0, "K must be a multiple of the group size"
+    if s_c is not None:
+        W = (W * np.asarray(s_c, dtype=np.float32)[None, :]).astype(np.float32)
+    G = K // GROUP
+    Wg = W.reshape(N, G, GROUP)
+    mn = Wg.min(axis=2)
+    mx = Wg.max(axis=2)
+    s32 = ((mx - mn) / np.float32(QMAX)).astype(np.float32)
+    s32 = np.minimum(np.maximum(s32, S_MIN), S_MAX)
+    s16 = s32.astype(np.float16)
+    s = s16.astype(np.float32)
+    z = np.clip(np.rint((-mn) / s), 0, QMAX).astype(np.float32)
+    q = np.clip(np.rint(Wg / s[:, :, None]) + z[:, :, None], 0, QMAX)
+    return (q.reshape(N, K).astype(np.uint8), z.astype(np.uint8), s16)
+
+
+# ------------------------------------------------------------ packing layout
+def pack_codes(q: np.ndarray) -> np.ndarray:
+    """8 codes per uint32: ``qweight[n, j]`` holds k = 8j+i in bits [4i, 4i+4).
+
+    [P5] 典型例子 names platform-aware weight packing without fixing a
+    layout; this layout is the library's documented canonical one.
+    """
+    q = np.asarray(q, dtype=np.uint32)
+    N, K = q.shape
+    q = q.reshape(N, K // 8, 8)
+    out = np.zeros((N, K // 8), dtype=np.uint32)
+    for i in range(8):
+        out |= q[:, :, i] << np.uint32(4 * i)
+    return out
+
+
+def unpack_codes(qweight: np.ndarray) -> np.ndarray:
+    qw = np.asarray(qweight, dtype=np.uint32)
+    N, J = qw.shape
+    out = np.empty((N, J, 8), dtype=np.uint8)
+    for i in range(8):
+        out[:, :, i] = (qw >> np.uint32(4 * i)) & np.uint32(0xF)
+    return out.reshape(N, J * 8)
+
+
+def pack_zeros(z: np.ndarray) -> np.ndarray:
+    """Zero points, 8 per uint32: group g = 8j+i in nibble i; pad nibbles = 0."""
+    z = np.asarray(z, dtype=np.uint32)
+    N, G = z.shape
+    J = (G + 7) // 8
+    zp = np.zeros((N, J * 8), dtype=np.uint32)
+    zp[:, :G] = z
+    return pack_codes(zp)
+
+
+def unpack_zeros(zeros: np.ndarray, G: int) -> np.ndarray:
+    return unpack_codes(zeros)[:, :G]
+
+
+def awq_pack(W16: np.ndarray, s_c: np.ndarray | None = None):
+    """Quantize and pack: returns ``qweight`` uint32 [N, K/8],
+    ``scales`` float16 [N, K/128], ``zeros`` uint32 [N, ceil(G/8)]."""
+    q, z, s16 = quantize(W16, s_c)
+    return pack_codes(q), s16, pack_zeros(z)
+
+
+# ------------------------------------------------------------ a4: dequant
+def dequant(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray) -> np.ndarray:
+    """``w^' = (q - z) * s`` in fp32 (exact: a 5-bit integer times an fp16).
+
+    [P4]: the int4 code is mapped back with its group's scale and zero point.
+    """
+    q = unpack_codes(qweight).astype(np.float32)
+    N, K = q.shape
+    G = K // GROUP
+    z = unpack_zeros(zeros, G).astype(np.float32)
+    s = np.asarray(scales, dtype=np.float16).astype(np.float32)
+    qg = q.reshape(N, G, GROUP)
+    return ((qg - z[:, :, None]) * s[:, :, None]).reshape(N, K).astype(np.float32)
+
+
+# ------------------------------------------------------ a7/a8: the linear
+def scaled_activations(X16: np.ndarray, inv_s: np.ndarray | None) -> np.ndarray:
+    """``x~ = fp32(x) * (1/s_c)`` rounded to fp32: the equivalent transformation
+    puts ``diag(1/s_c)`` on the activations ([P2] §2.2, [P5] 工作机制)."""
+    X = np.asarray(X16, dtype=np.float16).astype(np.float32)
+    if inv_s is None:
+        return X
+    return (X * np.asarray(inv_s, dtype=np.float32)[None, :]).astype(np.float32)
+
+
+def linear(X16, qweight, scales, zeros, inv_s=None):
+    """``Y^ = (X diag(1/s_c)) W^'^T`` summed in fp64.
+
+    Returns ``(Y, B)``: ``Y`` fp64 [M, N] and the tolerance base
+    ``B[m, n] = sum_k |x~_mk * w^'_nk|`` (fp64).
+    """
+    xt = scaled_activations(X16, inv_s).astype(np.float64)
+    wq = dequant(qweight, scales, zeros).astype(np.float64)
+    return xt @ wq.T, np.abs(xt) @ np.abs(wq).T
+
+
+def ulp_fp16(y: np.ndarray) -> np.ndarray:
+    """Spacing of fp16 numbers at |y| (2^-24 in the subnormal range)."""
+    a = np.abs(np.asarray(y, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -24)))
+    return np.exp2(np.maximum(e, -14.0) - 10.0)
+
+
+def tolerance(y_ref: np.ndarray, base: np.ndarray) -> np.ndarray:
+    """Per-element bound ``4e-3 * sum_k |x~ w^| + 1 fp16 ulp of y_ref``."""
+    return TOL_REL * np.asarray(base, dtype=np.float64) + ulp_fp16(y_ref)
+
+
+# --------------------------------------------------- a5/a6: alpha search
+def _reference_output(X16, W16, rows, t0, t1):
+    X = np.asarray(X16[t0:t1], dtype=np.float16).astype(np.float64)
+    Wr = np.asarray(W16, dtype=np.float16)[rows].astype(np.float64)
+    return X @ Wr.T
+
+
+def row_errors(X16, W16, s_c, inv_s, rows=None, token_chunk=4096):
+    """Per-output-row squared error ``e_n = sum_t (Y^_tn - Y_tn)^2`` (fp64)
+    for the scaled quantization of ``W`` with the given ``s_c``/``inv_s``.
+
+    ``Y = X W^T`` is the unquantized layer (READING: the fp16 weights, exact
+    sum); ``Y^`` is the quantized layer of :func:`linear`.  Only the listed
+    ``rows`` are evaluated (quantization is per row, so a row's codes do not
+    depend on the other rows).  The token sum is split into chunks only to
+    bound memory.
+    """
+    W16 = np.asarray(W16, dtype=np.float16)
+    N = W16.shape[0]
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    qw, sc, zs = awq_pack(W16[rows], s_c)
+    wq = dequant(qw, sc, zs).astype(np.float64)
+    T = X16.shape[0]
+    err = np.zeros(len(rows), dtype=np.float64)
+    for t0 in range(0, T, token_chunk):
+        t1 = min(T, t0 + token_chunk)
+        xt = scaled_activations(X16[t0:t1], inv_s).astype(np.float64)
+        r = xt @ wq.T - _reference_output(X16, W16, rows, t0, t1)
+        err += (r * r).sum(axis=0)
+    return err
+
+
+def search(X16, W16, n_grid: int = N_GRID, rows=None, a=None):
+    """Activation-aware scale search over ``alpha`` ([P2] §2.2, §3.3 第四步,
+    §5.1; [P5] 工作机制: no backpropagation, one coefficient per layer).
+
+    For each alpha_i in :func:`alpha_grid`: s_c = a^alpha_i, quantize
+    ``W diag(s_c)``, run the quantized layer on the calibration tokens and
+    score ``mse_i = sum (Y^ - Y)^2 / (T * N_rows)``.  alpha* = argmin, ties
+    broken by the smallest alpha (first index).
+
+    Returns a dict with ``mse`` [n_grid], ``row_err`` [n_grid, N_rows],
+    ``best`` (index), ``alpha``, ``s_c`` and ``inv_s`` of the best candidate.
+    """
+    X16 = np.asarray(X16, dtype=np.float16)
+    if a is None:
+        a = absmean(X16)
+    T = X16.shape[0]
+    W16 = np.asarray(W16, dtype=np.float16)
+    rows = np.arange(W16.shape[0]) if rows is None else np.asarray(rows)
+    alphas = alpha_grid(n_grid)
+    row_err = np.zeros((n_grid, len(rows)), dtype=np.float64)
+    for i, al in enumerate(alphas):
+        s_c, inv_s = channel_scales(a, al)
+        row_err[i] = row_errors(X16, W16, s_c, inv_s, rows)
+    mse = row_err.sum(axis=1) / (T * len(rows))
+    best = int(np.argmin(mse))
+    s_c, inv_s = channel_scales(a, alphas[best])
+    return {"mse": mse, "row_err": row_err, "best": best,
+            "alpha": float(alphas[best]), "s_c": s_c, "inv_s": inv_s, "a": a}
+
+
+def gram(X16, token_chunk=4096) -> np.ndarray:
+    """``H = X^T X`` in fp64 (K x K)."""
+    X16 = np.asarray(X16, dtype=np.float16)
+    K = X16.shape[1]
+    H = np.zeros((K, K), dtype=np.float64)
+    for t0 in range(0, X16.shape[0], token_chunk):
+        X = X16[t0:t0 + token_chunk].astype(np.float64)
+        H += X.T @ X
+    return H
+
+
+def row_errors_gram(H, W16, s_c, inv_s, rows=None):
+    """Second route to :func:`row_errors` through the identity
+    ``sum_t r_tn^2 = d_n^T H d_n`` with ``d_n = inv_s * w^'_n - w_n`` and
+    ``H = X^T X``.  Exact in real arithmetic when ``x~ = x * inv_s``; the
+    fp32 rounding of ``x~`` in :func:`row_errors` makes the two differ by a
+    few 1e-7 relative."""
+    W16 = np.asarray(W16, dtype=np.float16)
+    rows = np.arange(W16.shape[0]) if rows is None else np.asarray(rows)
+    qw, sc, zs = awq_pack(W16[rows], s_c)
+    wq = dequant(qw, sc, zs).astype(np.float64)
+    d = wq * np.asarray(inv_s, dtype=np.float64)[None, :] - W16[rows].astype(np.float64)
+    return np.einsum("nk,kj,nj->n", d, H, d)
