@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of the AWQ W4A16 linear layer on B300.
+
+Metric: W4A16 GEMV GB/s on Llama-2 shapes, as a fraction of the HBM roofline
+(the GEMM TFLOPS of the prefill shapes are reported beside it).
+
+Workload (one "step"): one decode token (M = 1) through the quantized linear
+layers of a 32-layer Llama-2-7B - per layer qkv 4096->12288, o 4096->4096,
+gate_up 4096->22016, down 11008->4096 - int4 codes, group 128, zero point,
+activation-aware channel scales folded into the activations.  Every layer
+has its own copy of the packed weights (3.4 GB per step, far above the
+126 MB L2), so every step streams its weights from HBM.  One step = 128
+launches of the library's GEMV, captured once in a CUDA graph.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 (torchrun, one rank per GPU) every rank runs the same workload on
+its own GPU (replicas; the layer is not sharded): value = total bytes of all
+ranks / max time over ranks.  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import awq_inputs  # noqa: E402
+
+MODEL = "llama2-7b"
+SHAPES = ["qkv", "o", "gate_up", "down"]
+PREFILL = [("llama2-7b", s) for s in SHAPES] + [("llama2-13b", s) for s in SHAPES]
+METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofline"
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
+
+
+def gemv_bytes(M, N, K):
+    """Algorithmic bytes of one W4A16 GEMV: codes, steps, zero points, x, inv_s, y."""
+    G = K // 128
+    return N * K // 2 + 2 * N * G + 4 * N * ((G + 7) // 8) + 2 * M * K + 4 * K + 2 * M * N
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML in a thread."""
+    NAMES = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+             0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks"}
+
+    def __init__(self, torch_dev):
+        self.samples, self.reasons = [], set()
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv = nv
+            props = __import__("torch").cuda.get_device_properties(torch_dev)
+            try:
+                bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id,
+                                            props.pci_device_id)
+                self.h = nv.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception:
+                self.h = nv.nvmlDeviceGetHandleByIndex(int(torch_dev))
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # NVML missing: clocks are reported as unavailable
+            self.err = repr(e)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.NAMES.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------- CPU oracle
+_ORACLE_WORK = {}
+
+
+def _oracle_work(rows_per_shape, M):
+    """Packs the sampled rows of each shape with the oracle (cached, untimed)."""
+    import oracle as O
+    key = (rows_per_shape, M)
+    if key not in _ORACLE_WORK:
+        work = []
+        for name in SHAPES:
+            K, N, lid = awq_inputs.layer(MODEL, name)
+            rows = np.linspace(0, N - 1, min(rows_per_shape, N)).astype(np.int64)
+            W = awq_inputs.weight(N, K, lid)[rows]
+            a = O.absmean(awq_inputs.calib_tokens(256, K, lid))
+            s_c, inv_s = O.channel_scales(a, 0.5)
+            qw, sc, zs = O.awq_pack(W, s_c)
+            X = awq_inputs.timed_tokens(M, K, lid)
+            work.append((X, qw, sc, zs, inv_s, gemv_bytes(M, len(rows), K)))
+        _ORACLE_WORK[key] = work
+    return _ORACLE_WORK[key]
+
+
+def oracle_sample(rows_per_shape, M=1, reps=1):
+    """Times the CPU oracle's quantized linear on ``rows_per_shape`` evenly
+    spaced output rows of each of the four shapes.  Returns (GB/s in the
+    metric's bytes, seconds, threads used, description)."""
+    import oracle as O
+    work = _oracle_work(rows_per_shape, M)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(reps):
+        for X, qw, sc, zs, inv_s, b in work:
+            O.linear(X, qw, sc, zs, inv_s)
+            nbytes += b
+    dt = time.perf_counter() - t0
+    try:
+        import threadpoolctl
+        threads = max(i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()) or 1
+    except Exception:
+        threads = os.cpu_count() or 1
+    desc = (f"oracle.linear (numpy, fp64 sums) on {rows_per_shape} evenly spaced output rows of "
+            f"each 7B shape, M={M}, x{reps}; weights packed outside the timing")
+    return nbytes / dt / 1e9, dt, threads, desc
+
+
+# ----------------------------------------------------------- GPU workload
+def build_workload(awq, torch, layers):
+    dev = torch.device("cuda")
+    shapes = []
+    for name in SHAPES:
+        K, N, lid = awq_inputs.layer(MODEL, name)
+        W = torch.from_numpy(awq_inputs.weight(N, K, lid)).to(dev)
+        Xc = torch.from_numpy(awq_inputs.calib_tokens(256, K, lid)).to(dev)
+        s_c, inv_s = awq.channel_scales(awq.absmean(Xc), 0.5)
+        qw, sc, zs = awq.pack(W, s_c)
+        del W, Xc
+        copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(layers - 1)]
+        shapes.append({"name": name, "K": K, "N": N, "inv_s": inv_s, "copies": copies,
+                       "bytes": gemv_bytes(1, N, K)})
+    # inputs and outputs of all launches live in two flat buffers (one copy each for e2e)
+    xin = sum(layers * s["K"] for s in shapes)
+    yout = sum(layers * s["N"] for s in shapes)
+    Xall = torch.empty(xin, dtype=torch.float16, device=dev)
+    Yall = torch.empty(yout, dtype=torch.float16, device=dev)
+    xo = yo = 0
+    calls = []
+    for l in range(layers):
+        for s in shapes:
+            K, N = s["K"], s["N"]
+            lid = awq_inputs.layer(MODEL, s["name"])[2]
+            Xall[xo:xo + K] = torch.from_numpy(awq_inputs.timed_tokens(1, K, lid)[0]).to(dev)
+            qw, sc, zs = s["copies"][l]
+            calls.append((Xall[xo:xo + K].view(1, K), qw, sc, zs, s["inv_s"], Yall[yo:yo + N].view(1, N), s))
+            xo += K
+            yo += N
+    return shapes, calls, Xall, Yall
+
+
+def run_step(awq, calls):
+    for X, qw, sc, zs, inv_s, Y, _ in calls:
+        awq.gemv(X, qw, sc, zs, inv_s, out=Y)
+
+
+def capture(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()   # warm-up outside capture (sets kernel attributes)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def gemm_prefill(awq, torch, pk, reps=5):
+    """TFLOPS of awq_gemm at M = 2048 and 4096 on the 7B and 13B shapes."""
+    dev = torch.device("cuda")
+    out = {}
+    gen = torch.Generator(device=dev)
+    total_flop = total_ms = 0.0
+    for model, name in PREFILL:
+        K, N, lid = awq_inputs.layer(model, name)
+        gen.manual_seed(1000 + lid)
+        W = (torch.randn((N, K), generator=gen, device=dev) * 0.02).half()
+        qw, sc, zs = awq.pack(W)
+        del W
+        for M in (2048, 4096):
+            gen.manual_seed(3000 + lid)
+            X = torch.randn((M, K), generator=gen, device=dev).half()
+            inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+            Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+            g = capture(torch, lambda: awq.gemm(X, qw, sc, zs, inv_s, out=Y, workspace=ws))
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            fl = 2.0 * M * N * K
+            out[f"{model}:{name}:M{M}"] = round(fl / ms / 1e9, 1)
+            total_flop += fl
+            total_ms += ms
+            del X, Y, ws, g
+        del qw, sc, zs
+    awq.check_device_error()
+    tf = total_flop / total_ms / 1e9
+    peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    return {"tflops": round(tf, 1), "peak_tflops": peak, "frac": round(tf / peak, 4),
+            "peak_note": "dense fp16 = measured bf16 cuBLAS burst x nominal fp16/bf16 ratio 1",
+            "per_shape_tflops": out, "includes": "X~ = fp16(X*inv_s) prescale + tcgen05 GEMM"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM figures")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    workload = (f"{MODEL} decode GEMV M=1, {args.layers} layers x (qkv 4096->12288, o 4096->4096, "
+                f"gate_up 4096->22016, down 11008->4096), int4 g128 zero point")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rows = 512
+        gbs = []
+        for _ in range(args.warmup):
+            oracle_sample(rows)
+        t_steps = []
+        for _ in range(args.steps):
+            g, dt, threads, desc = oracle_sample(rows)
+            gbs.append(g)
+            t_steps.append(dt)
+        ms = 1000 * sum(t_steps) / len(t_steps)
+        val = statistics.mean(gbs)
+        line = {"metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference",
+                "config": {"workload": workload, "sample": f"{rows} rows per shape per step"},
+                "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import weight_only_bit_05_b300 as awq
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    pk, pk_kind = peaks()
+    hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    shapes, calls, Xall, Yall = build_workload(awq, torch, args.layers)
+    step_bytes = sum(c[6]["bytes"] for c in calls)
+    graph = capture(torch, lambda: run_step(awq, calls))
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    t = torch.tensor([ms_total], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_total = float(t.item())
+    value = world * step_bytes * args.steps / (ms_total / 1000) / 1e9
+
+    # GEMV kernel timing, per shape: graph of that shape's launches over all layers
+    per_shape = {}
+    tot_b = tot_ms = 0.0
+    for s in shapes:
+        mine = [c for c in calls if c[6] is s]
+        g = capture(torch, lambda mine=mine: run_step(awq, mine))
+        g.replay()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, min(50, args.steps))
+        a0.record()
+        for _ in range(reps):
+            g.replay()
+        a1.record()
+        torch.cuda.synchronize()
+        us = a0.elapsed_time(a1) * 1000 / (reps * len(mine))
+        per_shape[s["name"]] = {"us_per_launch": round(us, 3), "GB/s": round(s["bytes"] / us / 1e3, 1)}
+        tot_b += s["bytes"]
+        tot_ms += us
+        del g
+    achieved = tot_b / tot_ms / 1e3
+
+    # end to end through the public API: host inputs in, host outputs out, every step
+    xh = torch.empty(Xall.shape, dtype=Xall.dtype, pin_memory=True)
+    xh.copy_(Xall)
+    yh = torch.empty(Yall.shape, dtype=Yall.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        Xall.copy_(xh, non_blocking=True)
+        run_step(awq, calls)
+        yh.copy_(Yall, non_blocking=True)
+    torch.cuda.synchronize()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record()
+    for _ in range(e2e_steps):
+        Xall.copy_(xh, non_blocking=True)
+        run_step(awq, calls)
+        yh.copy_(Yall, non_blocking=True)
+    b1.record()
+    torch.cuda.synchronize()
+    e2e_ms = b0.elapsed_time(b1) / e2e_steps
+    e2e = {"value": round(step_bytes / (e2e_ms / 1000) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": Xall.numel() * 2, "d2h_bytes_per_step": Yall.numel() * 2,
+           "path": "pinned host X -> awq.gemv x128 (eager, C ABI) -> pinned host Y"}
+
+    gemm = None if args.no_gemm else gemm_prefill(awq, torch, pk)
+    awq.check_device_error()
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu:
+        g, dt, threads, desc = oracle_sample(4096, reps=8)
+        cpu = {"value": round(g, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": desc + f"; {dt:.1f} s"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload, "M": 1, "layers": args.layers,
+                   "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2: every layer has its own packed weights "
+                         f"({step_bytes / 1e9:.2f} GB per step vs 126 MB L2)",
+                   "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "gemv_kernel<1> (awq_gemv)", "peak_kind": pk_kind,
+                     "per_shape": per_shape,
+                     "bytes_per_launch": {s["name"]: s["bytes"] for s in shapes}},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * len(calls),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gemm_prefill": gemm,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/*
+ * awq.h - C ABI of the B300 (sm_103a) AWQ W4A16 group-quantized linear layer.
+ *
+ * The method (Activation-aware Weight Quantization) as described by the pages
+ * "AWQ量化实战：无需重训，把大模型压进4bit显存" (§2.1-§2.3, §3.3),
+ * "大模型量化部署实战：GPTQ与AWQ算法" (section 大模型量化的核心原理与位宽选择)
+ * and "什么是激活感知权重量化（AWQ）？" (section 工作机制):
+ *
+ *   a_c    = mean_t |x_tc|                       per input channel (statistics)
+ *   s_c    = a_c ^ alpha,  alpha in {0, 1/20, ..., 19/20}
+ *   W'     = W diag(s_c)                          equivalent transformation
+ *   per (row n, group g of 128 input channels):   asymmetric round-to-nearest
+ *     s = fp16((max - min) / 15) clamped to [2^-14, 65504],
+ *     z = clamp(rint(-min / s), 0, 15),  q = clamp(rint(w' / s) + z, 0, 15)
+ *   w^'    = (q - z) * s                          dequantization
+ *   Y      = (X diag(1/s_c)) W^'^T                the quantized linear layer
+ *   alpha* = argmin over the grid of mean((Y - X W^T)^2) on calibration tokens
+ *
+ * Conventions for every entry point
+ *   - Matrices are row-major and dense. W is [N][K]: row n is output channel n,
+ *     column k is input channel k. X is [M][K] (tokens x input channels).
+ *   - fp16 data is passed as uint16_t bit patterns (IEEE binary16).
+ *   - Unless stated otherwise every pointer is a DEVICE pointer on the current
+ *     CUDA device, owned by the caller; the library never frees it and keeps no
+ *     reference after the call. Every device pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *     asynchronous on that stream unless stated otherwise.
+ *   - Shapes: K % 128 == 0, N % 8 == 0, M >= 1. The return value is a status
+ *     code below; on failure nothing was launched and
+ *     awq_last_error_string() (thread-local) says why.
+ *   - The library allocates no device memory on its own: kernels that need
+ *     scratch take a caller-provided workspace whose size the matching
+ *     *_workspace_size() function returns.
+ *
+ * Canonical packed layout (the library's own; the pages only name
+ * "platform-aware weight packing", "什么是激活感知权重量化（AWQ）？" 典型例子):
+ *   qweight uint32 [N][K/8]        : word j of row n holds k = 8j+i in bits [4i, 4i+4)
+ *   scales  fp16   [N][K/128]      : step of group g of row n
+ *   zeros   uint32 [N][ceil(G/8)]  : group g = 8j+i in bits [4i, 4i+4); unused nibbles 0
+ */
+#ifndef AWQ_H_
+#define AWQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define AWQ_API __attribute__((visibility("default")))
+#else
+#define AWQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define AWQ_OK              0
+#define AWQ_ERR_SHAPE       1  /* K % 128, N % 8, M or T out of range */
+#define AWQ_ERR_NULL        2  /* a required pointer is NULL */
+#define AWQ_ERR_ALIGN       3  /* a device pointer is not 16-byte aligned */
+#define AWQ_ERR_CUDA        4  /* a CUDA runtime/driver call failed */
+#define AWQ_ERR_UNSUPPORTED 5  /* configuration not implemented (w_bit, group, zero_point) */
+#define AWQ_ERR_WORKSPACE   6  /* workspace NULL, too small or misaligned */
+#define AWQ_ERR_DEVICE      7  /* a kernel reported a bounded wait that ran out */
+
+/* Quantization configuration ("awq-quantization" skill page, 步骤 2: zero_point,
+ * q_group_size, w_bit). Only w_bit = 4, group = 128, zero_point = 1 are
+ * implemented; n_grid is the number of alpha candidates (1..64, default 20). */
+typedef struct awq_config {
+  int32_t w_bit;
+  int32_t group;
+  int32_t zero_point;
+  int32_t n_grid;
+} awq_config;
+
+/* Default configuration {4, 128, 1, 20}. */
+AWQ_API awq_config awq_default_config(void);
+
+/* Human-readable reason of the last failing call on this host thread. */
+AWQ_API const char* awq_last_error_string(void);
+
+/* Reads and clears the device-side error word of the kernels that use bounded
+ * waits (the tensor-core matmul). Synchronizes `stream`. Returns AWQ_OK if no
+ * kernel reported a timeout since the last call, AWQ_ERR_DEVICE otherwise. */
+AWQ_API int awq_check_device_error(void* stream);
+
+/* ---------------------------------------------------------------- statistics
+ * a[c] = (1/T) * sum_t |X[t][c]|   ("AWQ量化实战" §2.1: mean absolute activation
+ * of each input channel over the calibration tokens).
+ * X: fp16 [T][K] device. a: fp32 [K] device (output).
+ * Sums are fp32 over runs of 16 tokens, then fp64; the result is
+ * deterministic (fixed reduction order).
+ * workspace: device, >= awq_absmean_workspace_size(T, K) bytes, 16-B aligned. */
+AWQ_API size_t awq_absmean_workspace_size(int64_t T, int32_t K);
+AWQ_API int awq_absmean(const uint16_t* X, int64_t T, int32_t K, float* a,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------- channel scales
+ * s_c[k] = fp32(pow(fp64(max(a[k], 1e-8f)), alpha)), inv_s[k] = 1.0f / s_c[k]
+ * (IEEE fp32 division). alpha must lie in [0, 1).
+ * ("AWQ量化实战" §2.2: salient channels are scaled up by a factor taken from the
+ * activation statistics.) a, s_c, inv_s: fp32 [K] device. */
+AWQ_API int awq_channel_scales(const float* a, int32_t K, double alpha, float* s_c,
+                       float* inv_s, void* stream);
+
+/* ---------------------------------------------------------------- quantizer
+ * Scaled group RTN with zero point and packing into the canonical layout
+ * ("AWQ量化实战" §1.1, §2.3; "大模型量化部署实战" 核心原理). Codes are decided in
+ * fp32 with IEEE division and round-half-even, bit-exact with the definition.
+ * W: fp16 [N][K]. s_c: fp32 [K] or NULL (all ones).
+ * qweight: uint32 [N][K/8]; scales: fp16 [N][K/128]; zeros: uint32 [N][ceil(G/8)]. */
+AWQ_API int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
+             const awq_config* cfg, uint32_t* qweight, uint16_t* scales,
+             uint32_t* zeros, void* stream);
+
+/* ------------------------------------------------------------ GEMV, M <= 8
+ * Y[m][n] = fp16( sum_k (X[m][k] * inv_s[k]) * (q[n][k] - z[n][g(k)]) * s[n][g(k)] )
+ * on CUDA cores: 128-bit loads of the packed codes, dequantization in
+ * registers, fp32 products and sums, warp-shuffle reductions; split-K is
+ * reduced inside a thread-block cluster through distributed shared memory.
+ * ("awq-quantization" skill page, 主要功能: the GEMV kernel serves batch-1
+ * token generation.)  X: fp16 [M][K], 1 <= M <= 8. inv_s: fp32 [K] or NULL
+ * (all ones). Y: fp16 [M][N]. */
+AWQ_API int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight,
+             const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
+             int32_t N, int32_t K, uint16_t* Y, void* stream);
+
+/* ------------------------------------------------------------- GEMM, any M
+ * Same result as awq_gemv for any M >= 1, on the 5th-generation tensor cores:
+ * packed codes and activations staged by TMA, codes dequantized to fp16 in
+ * shared memory, tcgen05.mma (fp16 x fp16, fp32 accumulation in tensor
+ * memory). ("awq-quantization" skill page, 主要功能: the GEMM kernel serves
+ * batch > 1.) When inv_s is not NULL, X~ = fp16(X * inv_s) is first written
+ * to the workspace; with inv_s == NULL X is read directly and the workspace
+ * may be NULL. Y: fp16 [M][N]. */
+AWQ_API size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K);
+AWQ_API int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight,
+             const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
+             int32_t N, int32_t K, uint16_t* Y, void* workspace,
+             size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ scale search
+ * The activation-aware grid search ("AWQ量化实战" §2.2, §3.3 第四步, §5.1: one
+ * coefficient per layer, no backpropagation): a = absmean(X_cal); for each
+ * alpha_i = i / n_grid: s_c = a^alpha_i, quantize W diag(s_c), run the
+ * quantized layer on the calibration tokens on the tensor cores and reduce
+ * mse_i = sum (Y^ - X_cal W^T)^2 / (T N) (fp32 per tile, fp64 across tiles).
+ * alpha* = first index of the smallest mse.
+ * X_cal: fp16 [T][K]; W: fp16 [N][K]; s_c_out, inv_s_out: fp32 [K] device
+ * (scales of the chosen alpha); best_out: HOST int32 (index of alpha*);
+ * mse_out: HOST double [n_grid]; row_err_out: DEVICE double [n_grid][N] or
+ * NULL (per-output-row squared error sums, for validation).
+ * Synchronizes `stream` (the host reads the n_grid errors). */
+AWQ_API size_t awq_search_workspace_size(int64_t T, int32_t N, int32_t K);
+AWQ_API int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* W,
+                      int32_t N, int32_t K, const awq_config* cfg,
+                      void* workspace, size_t ws_bytes, float* s_c_out,
+                      float* inv_s_out, int32_t* best_out, double* mse_out,
+                      double* row_err_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* AWQ_H_ */

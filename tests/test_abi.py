@@ -1,0 +1,99 @@
+"""The C-ABI library loads, exports every symbol include/awq.h declares, and
+rejects bad arguments on the host before touching a GPU (no compute call)."""
+import ctypes
+import re
+
+import pytest
+
+awq = pytest.importorskip("weight_only_bit_05_b300")
+lib = awq.lib
+
+AWQ_OK, AWQ_ERR_SHAPE, AWQ_ERR_NULL, AWQ_ERR_ALIGN = 0, 1, 2, 3
+AWQ_ERR_UNSUPPORTED, AWQ_ERR_WORKSPACE = 5, 6
+FAKE = 0x10000          # never dereferenced: validation fails first
+MIS = FAKE + 4          # misaligned pointer
+
+
+def test_every_declared_symbol_is_exported():
+    names = awq.exported_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_header_declares_what_the_binding_uses():
+    with open(awq.HEADER) as f:
+        txt = f.read()
+    for n in awq._SIGS:
+        assert re.search(r"\b%s\s*\(" % n, txt), n
+
+
+def test_default_config_and_workspace_sizes():
+    c = lib.awq_default_config()
+    assert (c.w_bit, c.group, c.zero_point, c.n_grid) == (4, 128, 1, 20)
+    assert lib.awq_gemm_workspace_size(16, 512, 512) == 16 * 512 * 2
+    assert lib.awq_gemm_workspace_size(0, 512, 512) == 0
+    assert lib.awq_absmean_workspace_size(4096, 4096) % 8 == 0
+    assert lib.awq_absmean_workspace_size(4096, 4096) >= 4096 * 8
+    ws = lib.awq_search_workspace_size(65536, 57344, 8192)
+    # Yref chunk <= 4 GiB, X~ 1 GiB, plus the packed chunk: a few GiB, not 15
+    assert (1 << 30) * 5 < ws < (1 << 30) * 7
+
+
+def _err():
+    return lib.awq_last_error_string().decode()
+
+
+def test_gemv_validation():
+    f = lib.awq_gemv
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 512, 100, FAKE, None) == AWQ_ERR_SHAPE
+    assert "multiple of 128" in _err()
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 12, 512, FAKE, None) == AWQ_ERR_SHAPE
+    assert f(FAKE, 9, FAKE, FAKE, FAKE, None, 512, 512, FAKE, None) == AWQ_ERR_SHAPE
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, None, 512, 512, FAKE, None) == AWQ_ERR_SHAPE
+    assert f(None, 1, FAKE, FAKE, FAKE, None, 512, 512, FAKE, None) == AWQ_ERR_NULL
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 512, 512, None, None) == AWQ_ERR_NULL
+    assert f(FAKE, 1, MIS, FAKE, FAKE, None, 512, 512, FAKE, None) == AWQ_ERR_ALIGN
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, MIS, 512, 512, FAKE, None) == AWQ_ERR_ALIGN
+
+
+def test_gemm_validation():
+    f = lib.awq_gemm
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, None, 512, 512, FAKE, None, 0, None) == AWQ_ERR_SHAPE
+    assert f(FAKE, 4, FAKE, FAKE, FAKE, None, 512, 384 + 64, FAKE, None, 0, None) == AWQ_ERR_SHAPE
+    # inv_s given: the workspace must hold X~
+    assert f(FAKE, 4, FAKE, FAKE, FAKE, FAKE, 512, 512, FAKE, None, 0, None) == AWQ_ERR_WORKSPACE
+    assert f(FAKE, 4, FAKE, FAKE, FAKE, FAKE, 512, 512, FAKE, FAKE, 100, None) == AWQ_ERR_WORKSPACE
+    assert f(FAKE, 4, FAKE, FAKE, FAKE, FAKE, 512, 512, FAKE, MIS, 1 << 20, None) == AWQ_ERR_WORKSPACE
+
+
+def test_pack_validation_and_config():
+    f = lib.awq_pack
+    cfg = lib.awq_default_config()
+    assert f(FAKE, None, 8, 100, ctypes.byref(cfg), FAKE, FAKE, FAKE, None) == AWQ_ERR_SHAPE
+    assert f(FAKE, None, 8, 128, ctypes.byref(cfg), None, FAKE, FAKE, None) == AWQ_ERR_NULL
+    for field, val in (("w_bit", 3), ("group", 64), ("zero_point", 0), ("n_grid", 0)):
+        bad = lib.awq_default_config()
+        setattr(bad, field, val)
+        assert f(FAKE, None, 8, 128, ctypes.byref(bad), FAKE, FAKE, FAKE, None) == AWQ_ERR_UNSUPPORTED
+
+
+def test_stats_and_search_validation():
+    assert lib.awq_absmean(FAKE, 0, 128, FAKE, FAKE, 1 << 20, None) == AWQ_ERR_SHAPE
+    assert lib.awq_absmean(FAKE, 16, 128, FAKE, None, 0, None) == AWQ_ERR_WORKSPACE
+    assert lib.awq_channel_scales(FAKE, 128, 1.0, FAKE, FAKE, None) == AWQ_ERR_SHAPE
+    assert lib.awq_channel_scales(FAKE, 128, -0.5, FAKE, FAKE, None) == AWQ_ERR_SHAPE
+    best = ctypes.c_int32()
+    mse = (ctypes.c_double * 20)()
+    cfg = lib.awq_default_config()
+    args = [FAKE, 256, FAKE, 512, 512, ctypes.byref(cfg), FAKE, 1 << 40, FAKE, FAKE,
+            ctypes.byref(best), mse, None, None]
+    bad = list(args)
+    bad[4] = 100
+    assert lib.awq_search_scales(*bad) == AWQ_ERR_SHAPE
+    bad = list(args)
+    bad[7] = 16
+    assert lib.awq_search_scales(*bad) == AWQ_ERR_WORKSPACE
+    bad = list(args)
+    bad[10] = None
+    assert lib.awq_search_scales(*bad) == AWQ_ERR_NULL

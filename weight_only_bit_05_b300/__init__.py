@@ -1,0 +1,196 @@
+"""Python binding of ``libawq.so``: the B300 AWQ W4A16 group-quantized linear.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch provides device memory and streams.  The library must have been built
+(``python weight_only_bit_05_b300/build.py``); importing this module without it
+raises, there is no fallback path.
+
+Functions take and return CUDA tensors on the current device and enqueue on
+the current torch stream:
+
+* ``absmean(X)``                      -> a fp32 [K]
+* ``channel_scales(a, alpha)``        -> (s_c, inv_s) fp32 [K]
+* ``pack(W, s_c=None)``               -> (qweight int32 [N, K/8], scales fp16 [N, K/128],
+                                          zeros int32 [N, ceil(G/8)])
+* ``gemv(X, qweight, scales, zeros, inv_s=None)``  M <= 8, CUDA cores
+* ``gemm(X, qweight, scales, zeros, inv_s=None)``  any M, tensor cores
+* ``search(X_cal, W, n_grid=20)``     -> dict(best, alpha, mse, s_c, inv_s, row_err)
+
+Packed integer tensors are int32 tensors holding the uint32 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+__all__ = ["lib", "LIB_PATH", "AwqError", "exported_symbols", "absmean", "channel_scales", "pack",
+           "gemv", "gemm", "search", "check_device_error", "gemm_workspace_bytes"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libawq.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "awq.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python weight_only_bit_05_b300/build.py` (nvcc, sm_103a)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+
+class AwqConfig(ctypes.Structure):
+    _fields_ = [("w_bit", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("zero_point", ctypes.c_int32), ("n_grid", ctypes.c_int32)]
+
+
+_p, _i32, _i64, _sz, _f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_double
+_SIGS = {
+    "awq_default_config": (AwqConfig, []),
+    "awq_last_error_string": (ctypes.c_char_p, []),
+    "awq_check_device_error": (ctypes.c_int, [_p]),
+    "awq_absmean_workspace_size": (_sz, [_i64, _i32]),
+    "awq_absmean": (ctypes.c_int, [_p, _i64, _i32, _p, _p, _sz, _p]),
+    "awq_channel_scales": (ctypes.c_int, [_p, _i32, _f64, _p, _p, _p]),
+    "awq_pack": (ctypes.c_int, [_p, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p, _p, _p, _p]),
+    "awq_gemv": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p]),
+    "awq_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "awq_gemm": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p, _sz, _p]),
+    "awq_search_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "awq_search_scales": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p,
+                                         _sz, _p, _p, ctypes.POINTER(ctypes.c_int32),
+                                         ctypes.POINTER(ctypes.c_double), _p, _p]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+STATUS = {0: "AWQ_OK", 1: "AWQ_ERR_SHAPE", 2: "AWQ_ERR_NULL", 3: "AWQ_ERR_ALIGN",
+          4: "AWQ_ERR_CUDA", 5: "AWQ_ERR_UNSUPPORTED", 6: "AWQ_ERR_WORKSPACE",
+          7: "AWQ_ERR_DEVICE"}
+
+
+class AwqError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def exported_symbols():
+    """Function names declared in include/awq.h."""
+    with open(HEADER) as f:
+        txt = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(awq_\w+)\s*\(", txt, re.M)))
+
+
+def _check(code: int):
+    if code != 0:
+        raise AwqError(code, lib.awq_last_error_string().decode())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _dev(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    return t
+
+
+def check_device_error():
+    _check(lib.awq_check_device_error(_stream()))
+
+
+def absmean(X: torch.Tensor) -> torch.Tensor:
+    _dev(X, torch.float16, "X")
+    T, K = X.shape
+    a = torch.empty(K, dtype=torch.float32, device=X.device)
+    ws = torch.empty(max(16, lib.awq_absmean_workspace_size(T, K)), dtype=torch.uint8, device=X.device)
+    _check(lib.awq_absmean(_ptr(X), T, K, _ptr(a), _ptr(ws), ws.numel(), _stream()))
+    return a
+
+
+def channel_scales(a: torch.Tensor, alpha: float):
+    _dev(a, torch.float32, "a")
+    K = a.numel()
+    s = torch.empty_like(a)
+    inv = torch.empty_like(a)
+    _check(lib.awq_channel_scales(_ptr(a), K, float(alpha), _ptr(s), _ptr(inv), _stream()))
+    return s, inv
+
+
+def pack(W: torch.Tensor, s_c: torch.Tensor | None = None):
+    _dev(W, torch.float16, "W")
+    if s_c is not None:
+        _dev(s_c, torch.float32, "s_c")
+    N, K = W.shape
+    G = K // 128
+    qweight = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((N, (G + 7) // 8), dtype=torch.int32, device=W.device)
+    cfg = lib.awq_default_config()
+    _check(lib.awq_pack(_ptr(W), _ptr(s_c), N, K, ctypes.byref(cfg), _ptr(qweight), _ptr(scales),
+                        _ptr(zeros), _stream()))
+    return qweight, scales, zeros
+
+
+def _linear_args(X, qweight, scales, zeros, inv_s):
+    _dev(X, torch.float16, "X")
+    _dev(qweight, torch.int32, "qweight")
+    _dev(scales, torch.float16, "scales")
+    _dev(zeros, torch.int32, "zeros")
+    if inv_s is not None:
+        _dev(inv_s, torch.float32, "inv_s")
+    M, K = X.shape
+    N = qweight.shape[0]
+    return M, N, K
+
+
+def gemv(X, qweight, scales, zeros, inv_s=None, out=None):
+    M, N, K = _linear_args(X, qweight, scales, zeros, inv_s)
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _check(lib.awq_gemv(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N, K,
+                        _ptr(Y), _stream()))
+    return Y
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib.awq_gemm_workspace_size(M, N, K))
+
+
+def gemm(X, qweight, scales, zeros, inv_s=None, out=None, workspace=None):
+    M, N, K = _linear_args(X, qweight, scales, zeros, inv_s)
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if inv_s is not None and workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=X.device)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.awq_gemm(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N, K,
+                        _ptr(Y), _ptr(workspace), nbytes, _stream()))
+    return Y
+
+
+def search(X_cal: torch.Tensor, W: torch.Tensor, n_grid: int = 20, row_err: bool = False):
+    _dev(X_cal, torch.float16, "X_cal")
+    _dev(W, torch.float16, "W")
+    T, K = X_cal.shape
+    N = W.shape[0]
+    ws = torch.empty(lib.awq_search_workspace_size(T, N, K), dtype=torch.uint8, device=W.device)
+    s_c = torch.empty(K, dtype=torch.float32, device=W.device)
+    inv_s = torch.empty(K, dtype=torch.float32, device=W.device)
+    rerr = torch.empty((n_grid, N), dtype=torch.float64, device=W.device) if row_err else None
+    best = ctypes.c_int32(-1)
+    mse = (ctypes.c_double * n_grid)()
+    cfg = lib.awq_default_config()
+    cfg.n_grid = n_grid
+    _check(lib.awq_search_scales(_ptr(X_cal), T, _ptr(W), N, K, ctypes.byref(cfg), _ptr(ws),
+                                 ws.numel(), _ptr(s_c), _ptr(inv_s), ctypes.byref(best), mse,
+                                 _ptr(rerr), _stream()))
+    return {"best": best.value, "alpha": best.value / n_grid, "mse": list(mse), "s_c": s_c,
+            "inv_s": inv_s, "row_err": rerr}

@@ -1,0 +1,253 @@
+// C-ABI entry points: argument validation, status codes and error strings.
+// Every step of the computation runs in the kernels of the other files.
+#include <cstdarg>
+#include <cstring>
+
+#include "awq_internal.h"
+
+namespace awq {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return AWQ_OK;
+  set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return AWQ_ERR_CUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t cols,
+                 uint64_t rows, uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the CUDA driver");
+    return AWQ_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (CUresult %d) for %llux%llu box %ux%u",
+              static_cast<int>(r), (unsigned long long)rows, (unsigned long long)cols, box_rows,
+              box_cols);
+    return AWQ_ERR_CUDA;
+  }
+  return AWQ_OK;
+}
+
+}  // namespace awq
+
+using namespace awq;
+
+namespace {
+
+int check_kn(int32_t N, int32_t K) {
+  if (K <= 0 || K % kGroup != 0) {
+    set_error("K = %d must be a positive multiple of 128", K);
+    return AWQ_ERR_SHAPE;
+  }
+  if (N <= 0 || N % 8 != 0) {
+    set_error("N = %d must be a positive multiple of 8", N);
+    return AWQ_ERR_SHAPE;
+  }
+  return AWQ_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+  if (!p) {
+    set_error("%s is NULL", name);
+    return AWQ_ERR_NULL;
+  }
+  if (!aligned16(p)) {
+    set_error("%s is not 16-byte aligned", name);
+    return AWQ_ERR_ALIGN;
+  }
+  return AWQ_OK;
+}
+
+int check_opt_ptr(const void* p, const char* name) { return p ? check_ptr(p, name) : AWQ_OK; }
+
+int check_cfg(const awq_config* cfg) {
+  if (!cfg) return AWQ_OK;  // NULL means the default configuration
+  if (cfg->w_bit != 4 || cfg->group != 128 || cfg->zero_point != 1) {
+    set_error("unsupported configuration w_bit=%d group=%d zero_point=%d (only 4/128/1)",
+              cfg->w_bit, cfg->group, cfg->zero_point);
+    return AWQ_ERR_UNSUPPORTED;
+  }
+  if (cfg->n_grid < 1 || cfg->n_grid > 64) {
+    set_error("n_grid = %d must be in [1, 64]", cfg->n_grid);
+    return AWQ_ERR_UNSUPPORTED;
+  }
+  return AWQ_OK;
+}
+
+#define AWQ_TRY(x)               \
+  do {                           \
+    int _s = (x);                \
+    if (_s != AWQ_OK) return _s; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+awq_config awq_default_config(void) {
+  awq_config c;
+  c.w_bit = 4;
+  c.group = 128;
+  c.zero_point = 1;
+  c.n_grid = 20;
+  return c;
+}
+
+const char* awq_last_error_string(void) { return g_err; }
+
+int awq_check_device_error(void* stream) {
+  unsigned flags = 0;
+  AWQ_TRY(read_clear_gemm_error(static_cast<cudaStream_t>(stream), &flags));
+  if (flags) {
+    set_error("a tensor-core matmul kernel gave up on a bounded wait (flags 0x%x)", flags);
+    return AWQ_ERR_DEVICE;
+  }
+  return AWQ_OK;
+}
+
+size_t awq_absmean_workspace_size(int64_t T, int32_t K) {
+  if (T <= 0 || K <= 0) return 0;
+  return absmean_workspace_size(T, K);
+}
+
+int awq_absmean(const uint16_t* X, int64_t T, int32_t K, float* a, void* workspace,
+                size_t ws_bytes, void* stream) {
+  if (T <= 0 || K <= 0 || K % kGroup != 0) {
+    set_error("awq_absmean: T = %lld must be >= 1 and K = %d a positive multiple of 128",
+              (long long)T, K);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(X, "X"));
+  AWQ_TRY(check_ptr(a, "a"));
+  if (!workspace || !aligned16(workspace) || ws_bytes < absmean_workspace_size(T, K)) {
+    set_error("awq_absmean: workspace must be 16-B aligned and >= %zu bytes",
+              absmean_workspace_size(T, K));
+    return AWQ_ERR_WORKSPACE;
+  }
+  return launch_absmean(reinterpret_cast<const __half*>(X), T, K, a, workspace,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int awq_channel_scales(const float* a, int32_t K, double alpha, float* s_c, float* inv_s,
+                       void* stream) {
+  if (K <= 0 || K % kGroup != 0) {
+    set_error("awq_channel_scales: K = %d must be a positive multiple of 128", K);
+    return AWQ_ERR_SHAPE;
+  }
+  if (!(alpha >= 0.0 && alpha < 1.0)) {
+    set_error("awq_channel_scales: alpha = %g must lie in [0, 1)", alpha);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(a, "a"));
+  AWQ_TRY(check_ptr(s_c, "s_c"));
+  AWQ_TRY(check_ptr(inv_s, "inv_s"));
+  return launch_channel_scales(a, K, alpha, s_c, inv_s, static_cast<cudaStream_t>(stream));
+}
+
+int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K, const awq_config* cfg,
+             uint32_t* qweight, uint16_t* scales, uint32_t* zeros, void* stream) {
+  AWQ_TRY(check_cfg(cfg));
+  AWQ_TRY(check_kn(N, K));
+  AWQ_TRY(check_ptr(W, "W"));
+  AWQ_TRY(check_opt_ptr(s_c, "s_c"));
+  AWQ_TRY(check_ptr(qweight, "qweight"));
+  AWQ_TRY(check_ptr(scales, "scales"));
+  AWQ_TRY(check_ptr(zeros, "zeros"));
+  return launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
+                     reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream));
+}
+
+int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
+             const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
+             void* stream) {
+  AWQ_TRY(check_kn(N, K));
+  if (M < 1 || M > 8) {
+    set_error("awq_gemv: M = %d must be in [1, 8]", M);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(X, "X"));
+  AWQ_TRY(check_ptr(qweight, "qweight"));
+  AWQ_TRY(check_ptr(scales, "scales"));
+  AWQ_TRY(check_ptr(zeros, "zeros"));
+  AWQ_TRY(check_opt_ptr(inv_s, "inv_s"));
+  AWQ_TRY(check_ptr(Y, "Y"));
+  return launch_gemv(reinterpret_cast<const __half*>(X), M, qweight,
+                     reinterpret_cast<const __half*>(scales), zeros, inv_s, N, K,
+                     reinterpret_cast<__half*>(Y), static_cast<cudaStream_t>(stream));
+}
+
+size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {
+  (void)N;
+  if (M <= 0 || K <= 0) return 0;
+  return ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256;
+}
+
+int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
+             const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
+             void* workspace, size_t ws_bytes, void* stream) {
+  AWQ_TRY(check_kn(N, K));
+  if (M < 1) {
+    set_error("awq_gemm: M = %d must be >= 1", M);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(X, "X"));
+  AWQ_TRY(check_ptr(qweight, "qweight"));
+  AWQ_TRY(check_ptr(scales, "scales"));
+  AWQ_TRY(check_ptr(zeros, "zeros"));
+  AWQ_TRY(check_opt_ptr(inv_s, "inv_s"));
+  AWQ_TRY(check_ptr(Y, "Y"));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const __half* xt = reinterpret_cast<const __half*>(X);
+  if (inv_s) {
+    if (!workspace || !aligned16(workspace) || ws_bytes < awq_gemm_workspace_size(M, N, K)) {
+      set_error("awq_gemm: workspace must be 16-B aligned and >= %zu bytes",
+                awq_gemm_workspace_size(M, N, K));
+      return AWQ_ERR_WORKSPACE;
+    }
+    __half* w = static_cast<__half*>(workspace);
+    AWQ_TRY(launch_prescale(xt, inv_s, M, K, w, st));
+    xt = w;
+  }
+  return launch_gemm(kGemmOutF16, xt, M, qweight, reinterpret_cast<const __half*>(scales), zeros,
+                     nullptr, N, K, Y, N, nullptr, 0, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,400 @@
+// W4A16 matmul on the 5th-generation tensor cores (tcgen05), any M.
+//
+// "awq-quantization（AWQ量化技术）Skill" page, section 主要功能和特点: the GEMM kernel
+// serves batch > 1 and prefill.  There the layer is a dense contraction, so
+// it runs on the tensor cores:
+//
+//   D[n][m] = sum_k W^'[n][k] * X~[m][k]       (MMA M = 128 weight rows,
+//                                               MMA N = BN tokens, K = 16/step)
+//
+// One CTA computes a 128 (output channels) x BN (tokens) tile of Y^T with
+// warp roles:
+//   warp 0      TMA producer: packed codes [128 rows x 8 words] and the
+//               activation tile [BN x 64] (128-byte swizzle) into an
+//               S-stage ring, completion counted on full[s];
+//   warp 1      allocates tensor memory and issues tcgen05.mma (one thread),
+//               releasing stage s through tcgen05.commit -> empty[s];
+//   warps 2..9  dequantize the stage's codes (w^ = (q - z) * s in half2,
+//               written to the 128-byte-swizzled K-major operand layout),
+//               fence the async proxy and arrive on deq[s]; after the main
+//               loop they read the fp32 accumulators from tensor memory
+//               (tcgen05.ld) and run the epilogue.
+// Putting the weights on the MMA's M side means every CTA dequantizes its
+// 128 x K weight tile exactly once per BN tokens, and small token counts
+// (BN = 16) waste no tensor-core work on padding.
+//
+// Every wait on an mbarrier is bounded (1 s); a wait that runs out records
+// the fact in a device word (read by awq_check_device_error), makes the
+// other roles stop, drains the copies and MMAs in flight, frees tensor
+// memory and returns.
+#include "awq_internal.h"
+
+namespace awq {
+
+__device__ unsigned int g_gemm_error = 0;
+
+namespace {
+
+constexpr int BM = 128;          // weight rows per CTA (MMA M)
+constexpr int BK = 64;           // K per stage: one 128-byte swizzle atom of fp16
+constexpr int kDeqWarps = 8;
+constexpr int kThreads = 64 + 32 * kDeqWarps;
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr int kSmemBudget = 227 * 1024 - 2048;
+
+template <int BN, int MODE>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int RAW_BYTES = (MODE == kGemmDenseF32) ? 0 : BM * BK / 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES + RAW_BYTES;
+  static constexpr int STAGES = (kSmemBudget / STAGE) > 8 ? 8 : (kSmemBudget / STAGE);
+  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 512;
+};
+
+struct Abort {
+  volatile int* flag;
+  __device__ bool raised() const { return *flag != 0; }
+  __device__ void raise(unsigned bit) const {
+    *flag = 1;
+    atomicOr(&g_gemm_error, bit);
+  }
+};
+
+// bounded wait that also gives up as soon as another role has aborted
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                              unsigned bit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (ab.raised()) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      ab.raise(bit);
+      return false;
+    }
+  }
+}
+
+// 8 codes of one word -> 8 fp16 weights in natural k order, (q - z) * s.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 zb, __half2 s2) {
+  // magic fp16 pairs 1024 + q: (k0,k4) (k1,k5) (k2,k6) (k3,k7)
+  const uint32_t h0 = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t h1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
+  const uint32_t h2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
+  const uint32_t h3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
+  uint32_t p[4];
+  p[0] = __byte_perm(h0, h1, 0x5410);   // (k0, k1)
+  p[1] = __byte_perm(h2, h3, 0x5410);   // (k2, k3)
+  p[2] = __byte_perm(h0, h1, 0x7632);   // (k4, k5)
+  p[3] = __byte_perm(h2, h3, 0x7632);   // (k6, k7)
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&p[i]), zb);   // q - z, exact
+    const __half2 v = __hmul2(d, s2);
+    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return out;
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_a,
+                const __half* __restrict__ scales, const uint32_t* __restrict__ zeros, int M,
+                int N, int K, void* __restrict__ out, int ldo, const float* __restrict__ yref,
+                int ldy) {
+  using C = Cfg<BN, MODE>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * C::A_BYTES;
+  uint8_t* sRaw = sB + S * C::B_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sRaw + S * C::RAW_BYTES);
+  uint64_t* deq = full + S;
+  uint64_t* empty = deq + S;
+  uint64_t* accum = empty + S;
+  uint64_t* drain = accum + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const Abort ab{abort_flag};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+  const int nk = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(deq + s, 32 * kDeqWarps);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(accum, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S;
+        if (kb >= S && !wait_or_abort(empty + s, ((kb / S) - 1) & 1, ab, 1u)) break;
+        mbar_arrive_expect_tx(full + s, (MODE == kGemmDenseF32 ? C::A_BYTES : C::RAW_BYTES) +
+                                            C::B_BYTES);
+        if (MODE == kGemmDenseF32)
+          tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
+        else
+          tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0);
+        tma_load_2d(sB + s * C::B_BYTES, &tm_b, full + s, kb * BK, m0);
+        issued = kb + 1;
+      }
+      // the copies still in flight complete before the CTA may exit
+      for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb) {
+        const int s = kb % S;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(full + s, (kb / S) & 1))
+          if (globaltimer_ns() - t0 > kWaitNs) {
+            ab.raise(16u);
+            break;
+          }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (kb / S) & 1;
+        if (!wait_or_abort(full + s, ph, ab, 2u)) break;
+        if (MODE != kGemmDenseF32 && !wait_or_abort(deq + s, ph, ab, 2u)) break;
+        tc_fence_after();
+        const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * C::A_BYTES));
+        const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * C::B_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+        umma_commit(empty + s);
+      }
+      umma_commit(accum);
+      umma_commit(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0))
+        if (globaltimer_ns() - t0 > kWaitNs) {
+          ab.raise(32u);
+          break;
+        }
+    }
+    __syncwarp();
+  } else {
+    const int d = warp - 2;   // 0..7
+    if (MODE != kGemmDenseF32) {
+      // ------------------------------------------------------------ dequant
+      const int r = (d & 3) * 32 + lane;   // tile row
+      const int half = d >> 2;             // words 4*half .. 4*half+3 of the stage
+      const int n = n0 + r;
+      const int G = K / kGroup, ZW = (G + 7) / 8;
+      const bool row_ok = n < N;
+      __half2 zb = __half2half2(__ushort_as_half(0x6400));
+      __half2 s2 = __half2half2(__ushort_as_half(0));
+      int cur_g = -1;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S;
+        const int g = (kb * BK) / kGroup;
+        if (g != cur_g) {
+          cur_g = g;
+          if (row_ok) {
+            const __half sv = scales[static_cast<size_t>(n) * G + g];
+            const uint32_t zw = __ldg(zeros + static_cast<size_t>(n) * ZW + (g >> 3));
+            const uint32_t z = (zw >> ((g & 7) * 4)) & 15u;
+            s2 = __half2half2(sv);
+            zb = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u | z)));
+          }
+        }
+        if (!wait_or_abort(full + s, (kb / S) & 1, ab, 4u)) break;
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(sRaw + s * C::RAW_BYTES + r * 32 + half * 16);
+        uint8_t* arow = sA + s * C::A_BYTES + r * 128;
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k
+          *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(rw[i], zb, s2);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(deq + s);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
+    const int colhalf = d >> 2;               // two warps per lane quarter
+    constexpr int kColsPerWarp = BN / 2 < 16 ? 16 : BN / 2;
+    const int c_begin = colhalf * kColsPerWarp;
+    const int n = n0 + quarter * 32 + lane;
+    float sq = 0.f;
+    if (c_begin < BN && wait_or_abort(accum, 0, ab, 8u)) {
+      tc_fence_after();
+      for (int c0 = c_begin; c0 < c_begin + kColsPerWarp; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c0 + j;
+          if (m < M && n < N) {
+            const float val = __uint_as_float(v[j]);
+            const size_t idx = static_cast<size_t>(m) * ldo + n;
+            if (MODE == kGemmOutF16) {
+              static_cast<__half*>(out)[idx] = __float2half_rn(val);
+            } else if (MODE == kGemmDenseF32) {
+              static_cast<float*>(out)[idx] = val;
+            } else {
+              const float e = val - yref[static_cast<size_t>(m) * ldy + n];
+              sq = fmaf(e, e, sq);
+            }
+          }
+        }
+      }
+    }
+    if (MODE == kGemmSqErr && n < N)
+      static_cast<float*>(out)[static_cast<size_t>(blockIdx.y * 2 + colhalf) * ldo + n] = sq;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+__global__ void prescale_kernel(const __half* __restrict__ X, const float* __restrict__ inv_s,
+                                int64_t total8, int K, __half* __restrict__ Xt) {
+  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (i >= total8) return;
+  const int k = static_cast<int>((i * 8) % K);
+  const uint4 xr = __ldg(reinterpret_cast<const uint4*>(X) + i);
+  const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
+  const float is[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const __half2* h = reinterpret_cast<const __half2*>(&xr);
+  uint4 o;
+  __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __half22float2(h[j]);
+    oh[j] = __halves2half2(__float2half_rn(__fmul_rn(f.x, is[2 * j])),
+                           __float2half_rn(__fmul_rn(f.y, is[2 * j + 1])));
+  }
+  reinterpret_cast<uint4*>(Xt)[i] = o;
+}
+
+template <int BN, int MODE>
+int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
+                const uint32_t* zeros, int M, int N, int K, void* out, int ldo, const float* yref,
+                int ldy, cudaStream_t st) {
+  using C = Cfg<BN, MODE>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    attr_set = true;
+  }
+  dim3 grid((N + BM - 1) / BM, (M + BN - 1) / BN, 1);
+  gemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, st>>>(tb, ta, scales, zeros, M, N, K, out, ldo,
+                                                         yref, ldy);
+  AWQ_CUDA_TRY_LAUNCH("gemm_kernel");
+  return AWQ_OK;
+}
+
+template <int MODE>
+int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
+                const uint32_t* zeros, int M, int N, int K, void* out, int ldo, const float* yref,
+                int ldy, cudaStream_t st) {
+  switch (bn) {
+    case 16: return launch_tile<16, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 32: return launch_tile<32, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 64: return launch_tile<64, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 128: return launch_tile<128, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    default: return launch_tile<256, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+  }
+}
+
+int pick_bn(int M, int mode) {
+  if (mode != kGemmOutF16) return 256;
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+}  // namespace
+
+int gemm_sqerr_slots(int M) { return ((M + 255) / 256) * 2; }
+
+int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
+                    cudaStream_t st) {
+  const int64_t total8 = M * K / 8;
+  const int threads = 256;
+  const int64_t blocks = (total8 + threads - 1) / threads;
+  prescale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(X, inv_s, total8, K, Xt);
+  AWQ_CUDA_TRY_LAUNCH("prescale_kernel");
+  return AWQ_OK;
+}
+
+int launch_gemm(int mode, const __half* Xt, int M, const uint32_t* qweight, const __half* scales,
+                const uint32_t* zeros, const __half* Wd, int N, int K, void* out, int ldo,
+                const float* yref, int ldy, cudaStream_t st) {
+  const int bn = pick_bn(M, mode);
+  CUtensorMap tb, ta;
+  int rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xt, K, M, static_cast<uint64_t>(K) * 2,
+                        BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != AWQ_OK) return rc;
+  if (mode == kGemmDenseF32)
+    rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Wd, K, N,
+                      static_cast<uint64_t>(K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, K / 8, N,
+                      static_cast<uint64_t>(K) / 2, BK / 8, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != AWQ_OK) return rc;
+  switch (mode) {
+    case kGemmOutF16:
+      return dispatch_bn<kGemmOutF16>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case kGemmSqErr:
+      return launch_tile<256, kGemmSqErr>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    default:
+      return launch_tile<256, kGemmDenseF32>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy,
+                                             st);
+  }
+}
+
+int read_clear_gemm_error(cudaStream_t st, unsigned* flags) {
+  AWQ_CUDA_TRY(cudaStreamSynchronize(st));
+  unsigned v = 0, zero = 0;
+  AWQ_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(v)));
+  AWQ_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(zero)));
+  *flags = v;
+  return AWQ_OK;
+}
+
+}  // namespace awq

@@ -1,0 +1,39 @@
+// Internal launchers behind the C ABI (C++ linkage, one per translation unit).
+// Arguments are already validated by the entry points in awq_api.cu.
+#pragma once
+
+#include "awq_common.cuh"
+
+namespace awq {
+
+// awq_stats.cu
+size_t absmean_workspace_size(int64_t T, int K);
+int launch_absmean(const __half* X, int64_t T, int K, float* a, void* ws, cudaStream_t st);
+int launch_channel_scales(const float* a, int K, double alpha, float* s_c, float* inv_s,
+                          cudaStream_t st);
+
+// awq_pack.cu
+int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweight,
+                __half* scales, uint32_t* zeros, cudaStream_t st);
+
+// awq_gemv.cu
+int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* scales,
+                const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
+                cudaStream_t st);
+
+// awq_gemm.cu
+enum GemmMode { kGemmOutF16 = 0, kGemmSqErr = 1, kGemmDenseF32 = 2 };
+int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
+                    cudaStream_t st);
+// Runs the tensor-core kernel on activations `Xt` [M][K] (already scaled).
+//   kGemmOutF16  : Y = fp16(Xt * dequant(qweight)^T), out = fp16 [M][ldo]
+//   kGemmSqErr   : out = fp32 partial sums of (Xt*dequant^T - yref)^2 per
+//                  output row, [ceil(M/256)*2][ldo]; yref fp32 [M][ldy]
+//   kGemmDenseF32: out = fp32 Xt * Wd^T, Wd fp16 [N][K] dense
+int launch_gemm(int mode, const __half* Xt, int M, const uint32_t* qweight, const __half* scales,
+                const uint32_t* zeros, const __half* Wd, int N, int K, void* out, int ldo,
+                const float* yref, int ldy, cudaStream_t st);
+int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
+int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
+
+}  // namespace awq
