@@ -83,7 +83,7 @@ class ClockSampler:
             self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
             self.ok = True
         except Exception as e:  # NVML missing: clocks are reported as unavailable
-            self.err = repr(e)
+            self.err = repr(e)[:200]
 
     def _run(self):
         nv = self.nv
@@ -111,7 +111,8 @@ class ClockSampler:
 
     def summary(self):
         if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"],
+                    "error": getattr(self, "err", "")}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
                 "samples": len(self.samples)}
@@ -256,6 +257,34 @@ def gemm_prefill(awq, torch, pk, reps=5):
             "per_shape_tflops": out, "includes": "X~ = fp16(X*inv_s) prescale + tcgen05 GEMM"}
 
 
+def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
+    """Wall time of awq_search_scales on one layer (20 alphas) and the
+    TFLOP/s of its tensor-core work (Y_ref once + 20 squared-error passes)."""
+    dev = torch.device("cuda")
+    K, N, lid = awq_inputs.layer(model, name)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + lid)
+    W = (torch.randn((N, K), generator=gen, device=dev) * 0.02).half()
+    gen.manual_seed(2000 + lid)
+    X = torch.randn((T, K), generator=gen, device=dev)
+    gen.manual_seed(4000 + lid)
+    idx = torch.randperm(K, generator=gen, device=dev)[:max(1, round(0.01 * K))]
+    X[:, idx] *= 20
+    X = X.half()
+    awq.search(X[:256].contiguous(), W[:1024].contiguous())   # warm-up (kernel attributes)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    res = awq.search(X, W)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    flop = 21 * 2.0 * T * N * K
+    del X, W
+    return {"layer": f"{model}:{name} {K}->{N}", "calib_tokens": T, "n_grid": 20,
+            "seconds": round(dt, 3), "tflops": round(flop / dt / 1e12, 1),
+            "alpha": res["alpha"], "includes": "statistics, 20x (pack, prescale, squared-error "
+                                               "GEMM, reductions), Y_ref GEMM, host argmin"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -265,6 +294,7 @@ def main():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-search", action="store_true", help="skip the scale-search timing")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -318,6 +348,14 @@ def main():
     graph = capture(torch, lambda: run_step(awq, calls))
     for _ in range(args.warmup):
         graph.replay()
+    # the GPU leaves its idle clocks only under sustained load: keep replaying
+    # (untimed) until at least 0.5 s of warm-up has passed
+    extra, t_end = 0, time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            graph.replay()
+        extra += 20
+        torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -380,6 +418,7 @@ def main():
            "path": "pinned host X -> awq.gemv x128 (eager, C ABI) -> pinned host Y"}
 
     gemm = None if args.no_gemm else gemm_prefill(awq, torch, pk)
+    search = None if args.no_search else search_run(awq, torch)
     awq.check_device_error()
 
     if rank != 0:
@@ -398,7 +437,8 @@ def main():
                    "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2: every layer has its own packed weights "
                          f"({step_bytes / 1e9:.2f} GB per step vs 126 MB L2)",
-                   "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events"},
+                   "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events",
+                   "extra_warmup_steps": extra},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": None,
                      "kernel": "gemv_kernel<1> (awq_gemv)", "peak_kind": pk_kind,
@@ -409,6 +449,7 @@ def main():
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gemm_prefill": gemm,
+        "search": search,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -41,3 +41,30 @@ def assert_linear_close(y_gpu: np.ndarray, X16, qw, sc, zs, inv_s, rows=None, co
     assert not bad.any(), (f"{int(bad.sum())} of {bad.size} outside the bound; worst ratio "
                            f"{float((err / tol).max()):.3f}")
     return float((err / tol).max())
+
+
+def row_sq_error_bound(X16, W16, s_c, inv_s, rows, e_ref, token_chunk=4096):
+    """Rigorous bound on |e_gpu - e_ref| per row for the squared-error pass.
+
+    The tensor cores multiply x~ and w^ rounded to fp16 (relative error
+    <= 2^-11 each) and accumulate K products in fp32; the reference output
+    X W^T is accumulated in fp32 too.  So every residual is off by at most
+    delta_t = u * (sum_k |x~ w^| + sum_k |x w|) with u = 2^-10 + K 2^-23, and
+    by Cauchy-Schwarz  |sum (r + d)^2 - sum r^2| <= 2 sqrt(e D) + D  with
+    D = sum_t delta_t^2.  The fp32 partial sums of squares (128 tokens each)
+    add at most 1e-5 e.
+    """
+    import oracle as O
+    W16 = np.asarray(W16, dtype=np.float16)
+    K = W16.shape[1]
+    qw, sc, zs = O.awq_pack(W16[rows], s_c)
+    aw = np.abs(O.dequant(qw, sc, zs).astype(np.float64))
+    ww = np.abs(W16[rows].astype(np.float64))
+    u = 2.0 ** -10 + K * 2.0 ** -23
+    D = np.zeros(len(rows))
+    for t0 in range(0, X16.shape[0], token_chunk):
+        xs = X16[t0:t0 + token_chunk]
+        b = np.abs(O.scaled_activations(xs, inv_s).astype(np.float64)) @ aw.T
+        b += np.abs(xs.astype(np.float64)) @ ww.T
+        D += ((u * b) ** 2).sum(axis=0)
+    return 2 * np.sqrt(e_ref * D) + D + 1e-5 * e_ref
