@@ -96,6 +96,22 @@ AWQ_API size_t awq_absmean_workspace_size(int64_t T, int32_t K);
 AWQ_API int awq_absmean(const uint16_t* X, int64_t T, int32_t K, float* a,
                 void* workspace, size_t ws_bytes, void* stream);
 
+/* Same statistics as awq_absmean for callers that cannot provide device memory:
+ * runtimes that plan every buffer before execution and forbid allocation on the
+ * execution path, real-time loops where an allocation's latency or failure is
+ * not acceptable, plugins whose host framework owns all device memory. The pages
+ * have no counterpart of this entry point; it exists for such callers only.
+ * The partial sums live in a fixed 4 MiB array of device memory inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. K is limited to 524288 input channels (larger K returns
+ * AWQ_ERR_SHAPE); T is not limited. The first call on a device looks up the
+ * array's device address on that device (call it once before any stream
+ * capture). Every call shares the one array: calls that overlap on the GPU
+ * (other streams, other threads) race and give wrong results; serialize them.
+ * No memory is allocated or freed by this call. X: fp16 [T][K], a: fp32 [K]. */
+AWQ_API int awq_absmean_noalloc(const uint16_t* X, int64_t T, int32_t K, float* a,
+                                void* stream);
+
 /* ----------------------------------------------------------- channel scales
  * s_c[k] = fp32(pow(fp64(max(a[k], 1e-8f)), alpha)), inv_s[k] = 1.0f / s_c[k]
  * (IEEE fp32 division). alpha must lie in [0, 1).

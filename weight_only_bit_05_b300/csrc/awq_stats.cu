@@ -4,6 +4,8 @@
 // channel is the mean of its absolute activations over many calibration
 // tokens.  §2.2: salient channels are multiplied by a factor derived from
 // that strength; the factor of every channel is a_c^alpha.
+#include <mutex>
+
 #include "awq_internal.h"
 
 namespace awq {
@@ -120,3 +122,87 @@ int launch_channel_scales(const float* a, int K, double alpha, float* s_c, float
 }
 
 }  // namespace awq
+
+// ------------------------------------------------------------------------
+// Statistics without any allocation by the caller or the library.
+//
+// Some callers cannot hand this library device memory at the point of the
+// call: runtimes that plan every buffer before execution and forbid
+// allocation on the execution path, real-time loops where an allocation's
+// latency or possible failure is not acceptable, and plugins whose host
+// framework owns all device memory and offers no workspace.  For them the
+// partial sums live in a fixed array in this file's device memory (4 MiB,
+// held by every GPU that loads the library until the process exits).
+namespace awq {
+namespace {
+
+constexpr size_t kNoAllocDoubles = (size_t(4) << 20) / sizeof(double);
+__device__ __align__(256) double g_absmean_scratch[kNoAllocDoubles];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+double* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the fixed array on the current device, looked up once
+// per device (the host-side name of the array is not a device address).
+int noalloc_scratch(double** out) {
+  int dev = 0;
+  AWQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("awq_absmean_noalloc: device ordinal %d >= %d is not supported", dev, kMaxDevices);
+    return AWQ_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_absmean_scratch);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(g_absmean_scratch)");
+    g_scratch_ptr[dev] = static_cast<double*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return AWQ_OK;
+}
+
+}  // namespace
+}  // namespace awq
+
+extern "C" AWQ_API int awq_absmean_noalloc(const uint16_t* X, int64_t T, int32_t K, float* a,
+                                           void* stream) {
+  using namespace awq;
+  if (T <= 0 || K <= 0 || K % kGroup != 0) {
+    set_error("awq_absmean_noalloc: T = %lld must be >= 1 and K = %d a positive multiple of 128",
+              (long long)T, K);
+    return AWQ_ERR_SHAPE;
+  }
+  if (static_cast<size_t>(K) > kNoAllocDoubles) {
+    set_error("awq_absmean_noalloc: K = %d exceeds the fixed scratch limit of %zu input channels",
+              K, kNoAllocDoubles);
+    return AWQ_ERR_SHAPE;
+  }
+  if (!X || !a) {
+    set_error("awq_absmean_noalloc: X and a must not be NULL");
+    return AWQ_ERR_NULL;
+  }
+  if (!aligned16(X) || !aligned16(a)) {
+    set_error("awq_absmean_noalloc: X and a must be 16-byte aligned");
+    return AWQ_ERR_ALIGN;
+  }
+  double* part = nullptr;
+  const int rc = noalloc_scratch(&part);
+  if (rc != AWQ_OK) return rc;
+  int splits = absmean_splits(T, K);
+  const int cap = static_cast<int>(kNoAllocDoubles / static_cast<size_t>(K));
+  if (splits > cap) splits = cap;
+  const int64_t per = (T + splits - 1) / splits;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dim3 grid((K / 8 + kColChunks - 1) / kColChunks, splits);
+  dim3 block(kColChunks, kTokLanes);
+  // every (split, column) slot that the finalize pass reads is written here,
+  // so nothing in the shared array needs clearing between calls
+  absmean_partial_kernel<<<grid, block, 0, st>>>(reinterpret_cast<const __half*>(X), T, K, per,
+                                                 part);
+  AWQ_CUDA_TRY_LAUNCH("absmean_partial_kernel");
+  absmean_finalize_kernel<<<(K + 255) / 256, 256, 0, st>>>(part, splits, K, T, a);
+  AWQ_CUDA_TRY_LAUNCH("absmean_finalize_kernel");
+  return AWQ_OK;
+}
