@@ -61,31 +61,37 @@ def peaks():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML in a thread."""
+    """Samples the SM clock and the clock-event reasons during the timed
+    region: through NVML when pynvml is importable, else by running
+    ``nvidia-smi --query-gpu ... -lms 50`` in the background."""
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     NAMES = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-             0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks"}
+             0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, torch_dev):
-        self.samples, self.reasons = [], set()
-        self.ok = False
+        import torch
+        self.samples, self.reasons, self.err = [], set(), ""
+        self.max_mhz, self.mode = None, None
         self._stop = threading.Event()
+        props = torch.cuda.get_device_properties(torch_dev)
+        try:
+            self.bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id,
+                                             props.pci_device_id)
+        except Exception:
+            self.bus = None
         try:
             import pynvml as nv
             nv.nvmlInit()
             self.nv = nv
-            props = __import__("torch").cuda.get_device_properties(torch_dev)
-            try:
-                bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id,
-                                            props.pci_device_id)
-                self.h = nv.nvmlDeviceGetHandleByPciBusId(bus)
-            except Exception:
-                self.h = nv.nvmlDeviceGetHandleByIndex(int(torch_dev))
+            self.h = (nv.nvmlDeviceGetHandleByPciBusId(self.bus) if self.bus
+                      else nv.nvmlDeviceGetHandleByIndex(int(torch_dev)))
             self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # NVML missing: clocks are reported as unavailable
-            self.err = repr(e)[:200]
+            self.mode = "nvml"
+        except Exception as e:
+            self.err = repr(e)[:120]
+            self.mode = "smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
@@ -99,23 +105,50 @@ class ClockSampler:
             time.sleep(0.002)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        else:
+            import subprocess
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "50"]
+            if self.bus:
+                cmd += ["-i", self.bus]
+            try:
+                self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                             text=True)
+            except Exception as e:
+                self.proc, self.err = None, self.err + " / " + repr(e)[:120]
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif getattr(self, "proc", None) is not None:
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(self.REASONS, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"],
-                    "error": getattr(self, "err", "")}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "error": self.err or "no samples"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.mode}
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -295,6 +328,8 @@ def main():
     ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-search", action="store_true", help="skip the scale-search timing")
+    ap.add_argument("--only-gemm", default=None, metavar="MODEL:LAYER:M",
+                    help="run only awq_gemm on one shape 3 times (a small case for profilers)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -333,6 +368,19 @@ def main():
     import torch
     import weight_only_bit_05_b300 as awq
     torch.cuda.set_device(local)
+    if args.only_gemm:
+        model, name, M = args.only_gemm.split(":")
+        K, N, lid = awq_inputs.layer(model, name)
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(1000 + lid)
+        qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device="cuda") * 0.02).half())
+        X = torch.randn((int(M), K), generator=gen, device="cuda").half()
+        inv_s = torch.ones(K, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            awq.gemm(X, qw, sc, zs, inv_s)
+        awq.check_device_error()
+        print("ok", args.only_gemm)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))

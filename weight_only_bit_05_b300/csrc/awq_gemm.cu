@@ -7,21 +7,25 @@
 //   D[n][m] = sum_k W^'[n][k] * X~[m][k]       (MMA M = 128 weight rows,
 //                                               MMA N = BN tokens, K = 16/step)
 //
-// One CTA computes a 128 (output channels) x BN (tokens) tile of Y^T with
-// warp roles:
+// The kernel is persistent: one CTA per SM walks the (128 output channels x
+// BN tokens) tiles of Y^T, with warp roles
 //   warp 0      TMA producer: packed codes [128 rows x 8 words] and the
 //               activation tile [BN x 64] (128-byte swizzle) into an
 //               S-stage ring, completion counted on full[s];
-//   warp 1      allocates tensor memory and issues tcgen05.mma (one thread),
-//               releasing stage s through tcgen05.commit -> empty[s];
-//   warps 2..9  dequantize the stage's codes (w^ = (q - z) * s in half2,
+//   warp 1      allocates tensor memory (two accumulators) and issues
+//               tcgen05.mma (one thread), releasing stage s through
+//               tcgen05.commit -> empty[s] and a finished accumulator through
+//               tcgen05.commit -> acc_full[b];
+//   warps 2..9  dequantize each stage's codes (w^ = (q - z) * s in half2,
 //               written to the 128-byte-swizzled K-major operand layout),
-//               fence the async proxy and arrive on deq[s]; after the main
-//               loop they read the fp32 accumulators from tensor memory
-//               (tcgen05.ld) and run the epilogue.
+//               fence the async proxy and arrive on deq[s];
+//   warps 10-13 epilogue: read a finished accumulator from tensor memory
+//               (tcgen05.ld), write the outputs and free it (acc_empty[b]),
+//               while the next tile accumulates into the other buffer.
 // Putting the weights on the MMA's M side means every CTA dequantizes its
 // 128 x K weight tile exactly once per BN tokens, and small token counts
-// (BN = 16) waste no tensor-core work on padding.
+// (BN = 16) waste no tensor-core work on padding.  Consecutive tiles of the
+// walk share the activation tile, which stays in L2.
 //
 // Every wait on an mbarrier is bounded (1 s); a wait that runs out records
 // the fact in a device word (read by awq_check_device_error), makes the
@@ -38,7 +42,8 @@ namespace {
 constexpr int BM = 128;          // weight rows per CTA (MMA M)
 constexpr int BK = 64;           // K per stage: one 128-byte swizzle atom of fp16
 constexpr int kDeqWarps = 8;
-constexpr int kThreads = 64 + 32 * kDeqWarps;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * (kDeqWarps + kEpiWarps);
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
@@ -49,7 +54,8 @@ struct Cfg {
   static constexpr int RAW_BYTES = (MODE == kGemmDenseF32) ? 0 : BM * BK / 2;
   static constexpr int STAGE = A_BYTES + B_BYTES + RAW_BYTES;
   static constexpr int STAGES = (kSmemBudget / STAGE) > 8 ? 8 : (kSmemBudget / STAGE);
-  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int ACC_COLS = BN < 32 ? 32 : BN;   // one fp32 accumulator
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;          // double-buffered
   static constexpr int SMEM = STAGES * STAGE + 1024 + 512;
 };
 
@@ -118,15 +124,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sRaw + S * C::RAW_BYTES);
   uint64_t* deq = full + S;
   uint64_t* empty = deq + S;
-  uint64_t* accum = empty + S;
-  uint64_t* drain = accum + 1;
+  uint64_t* acc_full = empty + S;     // [2]
+  uint64_t* acc_empty = acc_full + 2; // [2]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const Abort ab{abort_flag};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
   const int nk = K / BK;
+  const int n_tiles = (N + BM - 1) / BM;
+  const int tiles = n_tiles * ((M + BN - 1) / BN);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -134,7 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(deq + s, 32 * kDeqWarps);
       mbar_init(empty + s, 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);
+      mbar_init(acc_empty + b, 32 * kEpiWarps);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -149,28 +160,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched with programmatic stream serialization: the setup above may
+  // overlap the previous kernel; every global read comes after this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        if (kb >= S && !wait_or_abort(empty + s, ((kb / S) - 1) & 1, ab, 1u)) break;
-        mbar_arrive_expect_tx(full + s, (MODE == kGemmDenseF32 ? C::A_BYTES : C::RAW_BYTES) +
-                                            C::B_BYTES);
-        if (MODE == kGemmDenseF32)
-          tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
-        else
-          tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0);
-        tma_load_2d(sB + s * C::B_BYTES, &tm_b, full + s, kb * BK, m0);
-        issued = kb + 1;
+      int it = 0;   // k-blocks issued by this CTA over all its tiles
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int n0 = (t % n_tiles) * BM, m0 = (t / n_tiles) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if (it >= S && !wait_or_abort(empty + s, ((it / S) - 1) & 1, ab, 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full + s, (MODE == kGemmDenseF32 ? C::A_BYTES : C::RAW_BYTES) +
+                                              C::B_BYTES);
+          if (MODE == kGemmDenseF32)
+            tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
+          else
+            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0);
+          tma_load_2d(sB + s * C::B_BYTES, &tm_b, full + s, kb * BK, m0);
+        }
       }
       // the copies still in flight complete before the CTA may exit
-      for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb) {
-        const int s = kb % S;
+      for (int j = it > S ? it - S : 0; j < it; ++j) {
+        const int s = j % S;
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(full + s, (kb / S) & 1))
+        while (!mbar_try_wait(full + s, (j / S) & 1))
           if (globaltimer_ns() - t0 > kWaitNs) {
             ab.raise(16u);
             break;
@@ -182,20 +203,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
-        if (!wait_or_abort(full + s, ph, ab, 2u)) break;
-        if (MODE != kGemmDenseF32 && !wait_or_abort(deq + s, ph, ab, 2u)) break;
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        if (lt >= 2 && !wait_or_abort(acc_empty + b, ((lt >> 1) - 1) & 1, ab, 2u)) break;
         tc_fence_after();
-        const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * C::A_BYTES));
-        const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * C::B_BYTES));
+        const uint32_t d_tmem = tmem + b * C::ACC_COLS;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!wait_or_abort(full + s, ph, ab, 2u) ||
+              (MODE != kGemmDenseF32 && !wait_or_abort(deq + s, ph, ab, 2u))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * C::A_BYTES));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * C::B_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-        umma_commit(empty + s);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(empty + s);
+        }
+        if (ok) umma_commit(acc_full + b);
       }
-      umma_commit(accum);
       umma_commit(drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0))
@@ -205,57 +237,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncwarp();
-  } else {
-    const int d = warp - 2;   // 0..7
+  } else if (warp < 2 + kDeqWarps) {
+    // ------------------------------------------------------------ dequant
     if (MODE != kGemmDenseF32) {
-      // ------------------------------------------------------------ dequant
+      const int d = warp - 2;              // 0..7
       const int r = (d & 3) * 32 + lane;   // tile row
       const int half = d >> 2;             // words 4*half .. 4*half+3 of the stage
-      const int n = n0 + r;
       const int G = K / kGroup, ZW = (G + 7) / 8;
-      const bool row_ok = n < N;
-      __half2 zb = __half2half2(__ushort_as_half(0x6400));
-      __half2 s2 = __half2half2(__ushort_as_half(0));
-      int cur_g = -1;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        const int g = (kb * BK) / kGroup;
-        if (g != cur_g) {
-          cur_g = g;
-          if (row_ok) {
-            const __half sv = scales[static_cast<size_t>(n) * G + g];
-            const uint32_t zw = __ldg(zeros + static_cast<size_t>(n) * ZW + (g >> 3));
-            const uint32_t z = (zw >> ((g & 7) * 4)) & 15u;
-            s2 = __half2half2(sv);
-            zb = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u | z)));
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int n = (t % n_tiles) * BM + r;
+        const bool row_ok = n < N;
+        // step and zero point of the current group, and of the next one loaded
+        // a group (two stages) ahead so that the global-load latency is hidden
+        __half2 zb = __half2half2(__ushort_as_half(0x6400));
+        __half2 s2 = __half2half2(__ushort_as_half(0));
+        __half s_nx = __ushort_as_half(0);
+        uint32_t z_nx = 0;
+        if (row_ok) {
+          s_nx = scales[static_cast<size_t>(n) * G];
+          z_nx = __ldg(zeros + static_cast<size_t>(n) * ZW) & 15u;
+        }
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if ((kb * BK) % kGroup == 0) {
+            const int g = (kb * BK) / kGroup;
+            s2 = __half2half2(s_nx);
+            zb = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u | z_nx)));
+            if (row_ok && g + 1 < G) {
+              s_nx = scales[static_cast<size_t>(n) * G + g + 1];
+              z_nx = (__ldg(zeros + static_cast<size_t>(n) * ZW + ((g + 1) >> 3)) >>
+                      (((g + 1) & 7) * 4)) & 15u;
+            }
           }
-        }
-        if (!wait_or_abort(full + s, (kb / S) & 1, ab, 4u)) break;
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(sRaw + s * C::RAW_BYTES + r * 32 + half * 16);
-        uint8_t* arow = sA + s * C::A_BYTES + r * 128;
-        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          if (!wait_or_abort(full + s, (it / S) & 1, ab, 4u)) {
+            ok = false;
+            break;
+          }
+          const uint4 raw =
+              *reinterpret_cast<const uint4*>(sRaw + s * C::RAW_BYTES + r * 32 + half * 16);
+          uint8_t* arow = sA + s * C::A_BYTES + r * 128;
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k
-          *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(rw[i], zb, s2);
+          for (int i = 0; i < 4; ++i) {
+            const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k
+            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(rw[i], zb, s2);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(deq + s);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(deq + s);
       }
     }
+  } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
-    const int colhalf = d >> 2;               // two warps per lane quarter
-    constexpr int kColsPerWarp = BN / 2 < 16 ? 16 : BN / 2;
-    const int c_begin = colhalf * kColsPerWarp;
-    const int n = n0 + quarter * 32 + lane;
-    float sq = 0.f;
-    if (c_begin < BN && wait_or_abort(accum, 0, ab, 8u)) {
+    const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
+    int lt = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+      const int n0 = (t % n_tiles) * BM, mt = t / n_tiles, m0 = mt * BN;
+      const int b = lt & 1;
+      const int n = n0 + quarter * 32 + lane;
+      if (!wait_or_abort(acc_full + b, (lt >> 1) & 1, ab, 8u)) break;
       tc_fence_after();
-      for (int c0 = c_begin; c0 < c_begin + kColsPerWarp; c0 += 16) {
+      float sq = 0.f;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
+        tmem_ld16(tmem + b * C::ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -274,9 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (MODE == kGemmSqErr && n < N)
+        static_cast<float*>(out)[static_cast<size_t>(mt) * ldo + n] = sq;
+      tc_fence_before();
+      mbar_arrive(acc_empty + b);
     }
-    if (MODE == kGemmSqErr && n < N)
-      static_cast<float*>(out)[static_cast<size_t>(blockIdx.y * 2 + colhalf) * ldo + n] = sq;
   }
 
   tc_fence_before();
@@ -289,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 __global__ void prescale_kernel(const __half* __restrict__ X, const float* __restrict__ inv_s,
                                 int64_t total8, int K, __half* __restrict__ Xt) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (i >= total8) return;
   const int k = static_cast<int>((i * 8) % K);
@@ -319,10 +370,25 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr_set = true;
   }
-  dim3 grid((N + BM - 1) / BM, (M + BN - 1) / BN, 1);
-  gemm_kernel<BN, MODE><<<grid, kThreads, C::SMEM, st>>>(tb, ta, scales, zeros, M, N, K, out, ldo,
-                                                         yref, ldy);
-  AWQ_CUDA_TRY_LAUNCH("gemm_kernel");
+  cudaLaunchConfig_t cfg = {};
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    AWQ_CUDA_TRY(cudaGetDevice(&dev));
+    AWQ_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  }
+  const int tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
+  cfg.gridDim = dim3(tiles < sms ? tiles : sms, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE>, tb, ta, scales, zeros, M, N, K, out,
+                                  ldo, yref, ldy));
   return AWQ_OK;
 }
 
@@ -350,15 +416,23 @@ int pick_bn(int M, int mode) {
 
 }  // namespace
 
-int gemm_sqerr_slots(int M) { return ((M + 255) / 256) * 2; }
+int gemm_sqerr_slots(int M) { return (M + 255) / 256; }
 
 int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
                     cudaStream_t st) {
   const int64_t total8 = M * K / 8;
   const int threads = 256;
   const int64_t blocks = (total8 + threads - 1) / threads;
-  prescale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(X, inv_s, total8, K, Xt);
-  AWQ_CUDA_TRY_LAUNCH("prescale_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, prescale_kernel, X, inv_s, total8, K, Xt));
   return AWQ_OK;
 }
 

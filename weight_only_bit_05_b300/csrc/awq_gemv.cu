@@ -2,31 +2,34 @@
 //
 // "awq-quantization（AWQ量化技术）Skill" page, section 主要功能和特点: a GEMV kernel
 // serves batch-1 token generation; "AWQ量化实战" §3.4: decoding is bound by the
-// bandwidth of reading the weights.  At the B300's HBM rate an SM must retire
-// about 5.4 packed words (43 codes) per cycle, i.e. fewer than ~24 issue
-// slots per word and ~12 integer-pipe operations per word, so the kernel is
-// built around the instruction count per word:
+// bandwidth of reading the weights.  The kernel streams the packed codes from
+// HBM exactly once and hides the fixed cost of a launch behind that stream:
 //
-//  * codes become exact fp32 numbers with ONE LOP3 per code: the nibble at
-//    bit position p is OR-ed into the mantissa of 2^(23-p), giving
-//    2^(23-p) + q (p = 0, 4, 8 of the word and of the word >> 12, the shift
-//    done as a high multiply on the FMA pipe); four packed FADD2 remove the
-//    constant offsets, four packed FFMA2 accumulate x~ * q in fp32 (exact
-//    products of an fp32 activation and a 4-bit integer);
-//  * the zero point and the step are applied once per half group (8 words):
-//    y += s * (sum_k x~ q - z * sum_k x~), with the half-group sums of x~
-//    precomputed in shared memory;
-//  * a unit is R rows (4 at M = 1) x 16 groups: lane l reads 32 contiguous
-//    bytes (half a group) of each row, every activation vector read from
-//    shared memory serves R rows, and the next unit's codes are loaded into
-//    registers while the current one is computed;
-//  * one CTA per SM owns a balanced range of rows over the whole K; its warps
-//    take units from a shared-memory counter, each unit's row sums are
-//    reduced with warp shuffles into a per-(row, block) slot, and the slots
-//    are added in a fixed order (deterministic whatever warp took a unit);
-//  * only when the activations of a whole row do not fit in shared memory is
-//    K split across the CTAs of a thread-block cluster, reduced in rank order
-//    through distributed shared memory.
+//  * each CTA owns a balanced range of rows over the whole K; the rows of a
+//    range are contiguous in memory, so before anything else the CTA asks
+//    for its whole range (codes, steps, zero points) to be brought into L2
+//    with bulk prefetches.  The kernel is launched with programmatic stream
+//    serialization, so this starts while the previous kernel on the stream
+//    is still finishing; all loads proper come after griddepcontrol.wait
+//    (and see what that kernel wrote: the prefetch fills only the coherent L2);
+//  * a lane owns one whole group (16 words = 64 contiguous bytes, one step and
+//    one zero point) of a row per unit; a warp's unit is 32 consecutive groups
+//    of 2 rows, so each activation vector read from shared memory serves two
+//    rows;
+//  * the scaled activations x~ = fp16(fp32(x) * inv_s) are built once per CTA
+//    into shared memory, interleaved so that the 32 lanes read 32 consecutive
+//    16-byte vectors;
+//  * codes become fp16 numbers with one LOP3 per pair: 1024 + q for the even
+//    nibbles of a word and 64 + q for the odd nibbles (no shift needed for
+//    half of them); HSUB2 of the matching (1024 + z) or (64 + z) gives q - z
+//    exactly, and fma.rn.f32.f16 forms x~ (q - z) exactly in fp32 and adds it
+//    to fp32 accumulators; the group step multiplies each group's sum;
+//  * the 16 warps of a CTA split the CTA's (row pair, group block) units into
+//    contiguous runs, flush a row's sum with warp shuffles into a per-warp
+//    slot, and the slots are added in a fixed order (deterministic);
+//  * only when the activations of the whole K do not fit in shared memory is
+//    K split across the CTAs of a thread-block cluster, whose partial sums
+//    are added in rank order through distributed shared memory.
 #include <cooperative_groups.h>
 
 #include "awq_internal.h"
@@ -39,223 +42,209 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplit = 8;
-constexpr int kGroupsPerUnit = 16;                 // 32 lanes x half a group
-constexpr int kXsBudget = 160 * 1024;              // fp32 activation bytes per CTA
+constexpr int kXsBudget = 96 * 1024;   // activation bytes per CTA (2 CTAs per SM)
 
-template <uint32_t MASK>
-__device__ __forceinline__ float code_f32(uint32_t v, uint32_t magic) {
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t magic) {
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "n"(MASK), "r"(magic));
-  return __uint_as_float(d);
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
 }
 
-struct Magic {
-  uint32_t m23, m19, m15, m11, m7;   // bit patterns of 2^23, 2^19, 2^15, 2^11, 2^7
-  float2 o01, o23, o45, o67;         // minus the offsets of codes (0,1) (2,3) (4,5) (6,7)
-};
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
-// acc += x~[k0..k7] * q[k0..k7] for the 8 codes of word w; hi = w >> 12.
-__device__ __forceinline__ void word_dot(uint32_t w, uint32_t hi, const Magic& mg,
-                                         const float4& xa, const float4& xb, float2& acc) {
-  const float f0 = code_f32<0x0000000Fu>(w, mg.m23);    // 2^23 + q0
-  const float f1 = code_f32<0x000000F0u>(w, mg.m19);    // 2^19 + q1
-  const float f2 = code_f32<0x00000F00u>(w, mg.m15);    // 2^15 + q2
-  const float f3 = code_f32<0x0000000Fu>(hi, mg.m23);   // 2^23 + q3
-  const float f4 = code_f32<0x000000F0u>(hi, mg.m19);   // 2^19 + q4
-  const float f5 = code_f32<0x00000F00u>(hi, mg.m15);   // 2^15 + q5
-  const float f6 = code_f32<0x0000F000u>(hi, mg.m11);   // 2^11 + q6
-  const float f7 = code_f32<0x000F0000u>(hi, mg.m7);    // 2^7  + q7
-  const float2 q01 = __fadd2_rn(make_float2(f0, f1), mg.o01);
-  const float2 q23 = __fadd2_rn(make_float2(f2, f3), mg.o23);
-  const float2 q45 = __fadd2_rn(make_float2(f4, f5), mg.o45);
-  const float2 q67 = __fadd2_rn(make_float2(f6, f7), mg.o67);
-  acc = __ffma2_rn(make_float2(xa.x, xa.y), q01, acc);
-  acc = __ffma2_rn(make_float2(xa.z, xa.w), q23, acc);
-  acc = __ffma2_rn(make_float2(xb.x, xb.y), q45, acc);
-  acc = __ffma2_rn(make_float2(xb.z, xb.w), q67, acc);
+// c0 += a.lo * b.lo, c1 += a.hi * b.hi  (fp16 x fp16 exact, fp32 add)
+__device__ __forceinline__ void fma_mixed2(uint32_t a, uint32_t b, float& c0, float& c1) {
+  asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+      " fma.rn.f32.f16 %0, al, bl, %0;\n fma.rn.f32.f16 %1, ah, bh, %1;\n}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(a), "r"(b));
+}
+
+// x~ (q - z) for the 8 codes of one word into four fp32 accumulators.
+// x holds the activations as fp16 pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+__device__ __forceinline__ void word_dot(uint32_t w, uint32_t zb_even, uint32_t zb_odd,
+                                         const uint4& x, float (&c)[4]) {
+  const uint32_t t = w >> 8;
+  const uint32_t d0 = hsub2_u(and_or(w, 0x000F000Fu, 0x64006400u), zb_even);   // (k0, k4)
+  const uint32_t d1 = hsub2_u(and_or(w, 0x00F000F0u, 0x54005400u), zb_odd);    // (k1, k5)
+  const uint32_t d2 = hsub2_u(and_or(t, 0x000F000Fu, 0x64006400u), zb_even);   // (k2, k6)
+  const uint32_t d3 = hsub2_u(and_or(t, 0x00F000F0u, 0x54005400u), zb_odd);    // (k3, k7)
+  fma_mixed2(d0, x.x, c[0], c[1]);
+  fma_mixed2(d1, x.y, c[2], c[3]);
+  fma_mixed2(d2, x.z, c[0], c[1]);
+  fma_mixed2(d3, x.w, c[2], c[3]);
+}
+
+// Bulk L2 prefetch of [p, p + bytes) in pieces of at most 64 KB, spread over
+// the lanes of the calling warp.
+__device__ __forceinline__ void prefetch_range(const void* p, size_t bytes, int lane) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(15);
+  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~static_cast<uintptr_t>(15);
+  constexpr uintptr_t kPiece = 65536;
+  for (uintptr_t a = a0 + lane * kPiece; a < a1; a += 32 * kPiece) {
+    const uintptr_t e = a + kPiece < a1 ? a + kPiece : a1;
+    prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
+  }
 }
 
 template <int MM, int R>
-struct UnitRegs {
-  uint4 w[R][2];      // 8 packed words of each row
-  float s[R];         // group step
-  float z[R];         // zero point
-};
-
-template <int MM, int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
     gemv_kernel(const __half* __restrict__ X, const uint32_t* __restrict__ qweight,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros,
                 const float* __restrict__ inv_s, int N, int K, int KS, int rows_cap,
-                uint32_t hi_mult, __half* __restrict__ Y) {
-  extern __shared__ float4 smem_f4[];
-  __shared__ int next_unit;
+                __half* __restrict__ Y) {
+  extern __shared__ uint4 smem_u4[];
   const int kbeg = blockIdx.y * KS;
-  const int klen = min(K - kbeg, KS);              // multiple of 128
-  const int Gs = klen / kGroup;
-  // B: blocks of 16 groups in this slice; the shared-memory layout uses Bl,
-  // the block count of a full slice, so that it is the same in every rank
-  const int B = (Gs + kGroupsPerUnit - 1) / kGroupsPerUnit;
-  const int Bl = (KS / kGroup + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int klen = min(K - kbeg, KS);          // multiple of 128
+  const int Gs = klen / kGroup;                // groups in the slice
+  const int B = (Gs + 31) / 32;                // group blocks of 32 (one per lane)
   const int gbeg = kbeg / kGroup;
-  float4* xs = smem_f4;                                       // [MM][Bl][8 words][2][32]
-  float* xsum = reinterpret_cast<float*>(xs + static_cast<size_t>(MM) * Bl * 512);   // [MM][Bl][32]
-  float* part = xsum + static_cast<size_t>(MM) * Bl * 32;     // [MM][rows_cap][Bl]
+  uint4* xs = smem_u4;                         // [MM][B*16][32]
+  float* red = reinterpret_cast<float*>(xs + static_cast<size_t>(MM) * B * 512);   // [MM][kWarps][rows_cap]
 
-  // rows of this CTA: whole units of R rows, balanced over gridDim.x
+  // rows of this CTA (whole units of R rows, balanced over gridDim.x)
   const int NU = N / R;
-  const int q0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * NU / gridDim.x);
-  const int q1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * NU / gridDim.x);
-  const int row_base = q0 * R;
-  const int nunits = (q1 - q0) * B;
+  const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * NU / gridDim.x);
+  const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * NU / gridDim.x);
+  const int row_base = u0 * R;
+  const int nrows = (u1 - u0) * R;
   const int G = K / kGroup, ZW = (G + 7) / 8, KW = K / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // unit u -> (row unit, block); lane -> half group
-  auto issue = [&](int u, UnitRegs<MM, R>& ur) {
-    const int qu = u / B, b = u - qu * B;
-    const int gl = b * kGroupsPerUnit + (lane >> 1);
-    if (gl < Gs) {
-      const int g = gbeg + gl;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int row = row_base + qu * R + r;
-        const uint4* src = reinterpret_cast<const uint4*>(qweight + static_cast<size_t>(row) * KW +
-                                                          g * 16 + (lane & 1) * 8);
-        ur.w[r][0] = __ldg(src);
-        ur.w[r][1] = __ldg(src + 1);
-        ur.s[r] = __half2float(scales[static_cast<size_t>(row) * G + g]);
-        const uint32_t zw = __ldg(zeros + static_cast<size_t>(row) * ZW + (g >> 3));
-        ur.z[r] = static_cast<float>((zw >> ((g & 7) * 4)) & 15u);
-      }
-    }
-  };
-
-  // the first unit's codes are requested before the activations are staged
-  UnitRegs<MM, R> cur, nxt;
-  int u = warp < nunits ? warp : nunits;
-  if (u < nunits) issue(u, cur);
-  if (threadIdx.x == 0) next_unit = kWarps;
-
-  // ---- prologue: x~ = fp32(x) * inv_s into shared memory, half-group sums
-  const int nw = klen / 8;
-  for (int base = (threadIdx.x & ~31); base < MM * nw; base += kThreads) {
-    const int idx = base + lane;
-    const bool ok = idx < MM * nw;
-    float f[8];
-    float sum = 0.f;
-    int m = 0, c = 0;
-    if (ok) {
-      m = idx / nw;
-      c = idx - m * nw;
-      const uint4 xr = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + kbeg + 8 * c));
-      const __half2* xh = reinterpret_cast<const __half2*>(&xr);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 v = __half22float2(xh[i]);
-        f[2 * i] = v.x;
-        f[2 * i + 1] = v.y;
-      }
-      if (inv_s) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + kbeg + 8 * c));
-        const float4 bq = __ldg(reinterpret_cast<const float4*>(inv_s + kbeg + 8 * c + 4));
-        const float is[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], is[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sum += f[i];
-      // word c: half group hg = c / 8 (lane of the unit = hg % 32), word j = c % 8
-      const int hg = c >> 3, j = c & 7, b = hg >> 5, l = hg & 31;
-      float4* dst = xs + ((static_cast<size_t>(m) * Bl + b) * 8 + j) * 64 + l;
-      dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-      dst[32] = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    // half-group sum over the 8 consecutive words (lanes 8i..8i+7)
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-    if (ok && (c & 7) == 0) {
-      const int hg = c >> 3;
-      xsum[(static_cast<size_t>(m) * Bl + (hg >> 5)) * 32 + (hg & 31)] = sum;
-    }
+  // ---- start streaming this CTA's rows into L2 (before the dependency wait)
+  if (warp == 0) {
+    prefetch_range(qweight + static_cast<size_t>(row_base) * KW, static_cast<size_t>(nrows) * KW * 4, lane);
+  } else if (warp == 1) {
+    prefetch_range(scales + static_cast<size_t>(row_base) * G, static_cast<size_t>(nrows) * G * 2, lane);
+    prefetch_range(zeros + static_cast<size_t>(row_base) * ZW, static_cast<size_t>(nrows) * ZW * 4, lane);
   }
-  for (int i = threadIdx.x; i < MM * rows_cap * Bl; i += kThreads) part[i] = 0.f;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // ---- prologue: x~ into shared memory, zero the per-warp row slots
+  const int nw = klen / 8;   // packed words per row in the slice
+  for (int idx = threadIdx.x; idx < MM * nw; idx += kThreads) {
+    const int m = idx / nw, c = idx - m * nw;
+    const int gl = c >> 4, j = c & 15, b = gl >> 5, l = gl & 31;
+    const size_t xo = static_cast<size_t>(m) * K + kbeg + 8 * c;
+    const uint4 xr = __ldg(reinterpret_cast<const uint4*>(X + xo));
+    const __half2* xh = reinterpret_cast<const __half2*>(&xr);
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = __half22float2(xh[i]);
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+    if (inv_s) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + kbeg + 8 * c));
+      const float4 bq = __ldg(reinterpret_cast<const float4*>(inv_s + kbeg + 8 * c + 4));
+      const float is[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], is[i]);
+    }
+    uint4 o;
+    __half2 p;
+    p = __halves2half2(__float2half_rn(f[0]), __float2half_rn(f[4])); o.x = *reinterpret_cast<uint32_t*>(&p);
+    p = __halves2half2(__float2half_rn(f[1]), __float2half_rn(f[5])); o.y = *reinterpret_cast<uint32_t*>(&p);
+    p = __halves2half2(__float2half_rn(f[2]), __float2half_rn(f[6])); o.z = *reinterpret_cast<uint32_t*>(&p);
+    p = __halves2half2(__float2half_rn(f[3]), __float2half_rn(f[7])); o.w = *reinterpret_cast<uint32_t*>(&p);
+    xs[(static_cast<size_t>(m) * B + b) * 512 + j * 32 + l] = o;
+  }
+  for (int i = threadIdx.x; i < MM * kWarps * rows_cap; i += kThreads) red[i] = 0.f;
   __syncthreads();
 
-  Magic mg;
-  mg.m23 = 0x4B000000u;
-  mg.m19 = 0x49000000u;
-  mg.m15 = 0x47000000u;
-  mg.m11 = 0x45000000u;
-  mg.m7 = 0x43000000u;
-  mg.o01 = make_float2(-8388608.f, -524288.f);
-  mg.o23 = make_float2(-32768.f, -8388608.f);
-  mg.o45 = make_float2(-524288.f, -32768.f);
-  mg.o67 = make_float2(-2048.f, -128.f);
+  // ---- main loop over this warp's contiguous run of (row unit, group block)
+  const int nunits = (u1 - u0) * B;
+  const int ub = static_cast<int>(static_cast<int64_t>(warp) * nunits / kWarps);
+  const int ue = static_cast<int>(static_cast<int64_t>(warp + 1) * nunits / kWarps);
 
-  // ---- main loop: dynamic units, next unit's codes in flight during compute
-  while (u < nunits) {
-    int un = 0;
-    if (lane == 0) un = atomicAdd(&next_unit, 1);
-    un = __shfl_sync(0xffffffffu, un, 0);
-    if (un < nunits) issue(un, nxt);
-
-    const int qu = u / B, b = u - qu * B;
-    const int gl = b * kGroupsPerUnit + (lane >> 1);
-    float res[R][MM];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int m = 0; m < MM; ++m) res[r][m] = 0.f;
-    if (gl < Gs) {
-#pragma unroll
-      for (int m = 0; m < MM; ++m) {
-        const float4* xp = xs + (static_cast<size_t>(m) * Bl + b) * 512 + lane;
-        float2 acc[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) acc[r] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 xa = xp[j * 64];
-          const float4 xb = xp[j * 64 + 32];
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const uint4& q4 = cur.w[r][j >> 2];
-            const uint32_t w = (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
-            word_dot(w, __umulhi(w, hi_mult), mg, xa, xb, acc[r]);
-          }
-        }
-        const float xsm = xsum[(static_cast<size_t>(m) * Bl + b) * 32 + lane];
-#pragma unroll
-        for (int r = 0; r < R; ++r) res[r][m] = cur.s[r] * ((acc[r].x + acc[r].y) - cur.z[r] * xsm);
-      }
-    }
+  float acc[R][MM];
+  int cur = -1;
+  auto flush = [&](int unit_row) {
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int m = 0; m < MM; ++m) {
-        float v = res[r][m];
+        float v = acc[r][m];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) part[(static_cast<size_t>(m) * rows_cap + qu * R + r) * Bl + b] = v;
+        if (lane == 0) red[(m * kWarps + warp) * rows_cap + unit_row * R + r] = v;
       }
-    u = un;
-    cur = nxt;
+  };
+
+  for (int u = ub; u < ue; ++u) {
+    const int ul = u / B, b = u - ul * B;
+    if (ul != cur) {
+      if (cur >= 0) flush(cur);
+      cur = ul;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MM; ++m) acc[r][m] = 0.f;
+    }
+    const int gl = b * 32 + lane;
+    if (gl < Gs) {
+      const int g = gbeg + gl;
+      uint4 wq[R][4];
+      float s[R];
+      uint32_t zbe[R], zbo[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = row_base + ul * R + r;
+        const uint4* src = reinterpret_cast<const uint4*>(qweight + static_cast<size_t>(row) * KW + g * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) wq[r][v] = __ldg(src + v);
+        s[r] = __half2float(scales[static_cast<size_t>(row) * G + g]);
+        const uint32_t z = (__ldg(zeros + static_cast<size_t>(row) * ZW + (g >> 3)) >> ((g & 7) * 4)) & 15u;
+        zbe[r] = (0x6400u | z) * 0x00010001u;          // (1024 + z, 1024 + z)
+        zbo[r] = (0x5400u | (z << 4)) * 0x00010001u;   // (64 + z, 64 + z)
+      }
+      float c[R][MM][4];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MM; ++m)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) c[r][m][i] = 0.f;
+      const uint4* xp = xs + static_cast<size_t>(b) * 512 + lane;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+#pragma unroll
+        for (int m = 0; m < MM; ++m) {
+          const uint4 xv = xp[static_cast<size_t>(m) * B * 512 + j * 32];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const uint4& q4 = wq[r][j >> 2];
+            const uint32_t w = (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
+            word_dot(w, zbe[r], zbo[r], xv, c[r][m]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MM; ++m)
+          acc[r][m] = fmaf(s[r], (c[r][m][0] + c[r][m][1]) + (c[r][m][2] + c[r][m][3]), acc[r][m]);
+    }
   }
+  if (cur >= 0) flush(cur);
   __syncthreads();
 
-  // ---- fixed-order sums over the group blocks; cluster reduction over K slices
-  const int nrows = (q1 - q0) * R;
+  // ---- fixed-order sum of the per-warp slots; cluster reduction over K slices
+  float* total = red;   // warp 0's slots hold the CTA total in the cluster case
   for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
     const int m = i / nrows, rl = i - m * nrows;
-    const float* p = part + (static_cast<size_t>(m) * rows_cap + rl) * Bl;
     float v = 0.f;
-    for (int b = 0; b < B; ++b) v += p[b];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v += red[(m * kWarps + w) * rows_cap + rl];
     if (gridDim.y == 1)
       Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
     else
-      part[(static_cast<size_t>(m) * rows_cap + rl) * Bl] = v;   // slot 0 holds the row total
+      total[m * kWarps * rows_cap + rl] = v;   // only the slot read by this thread changes
   }
   if (gridDim.y == 1) return;
   cg::cluster_group cluster = cg::this_cluster();
@@ -263,10 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cluster.block_rank() == 0) {
     for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
       const int m = i / nrows, rl = i - m * nrows;
-      const size_t slot = (static_cast<size_t>(m) * rows_cap + rl) * Bl;
       float v = 0.f;
       for (int rk = 0; rk < static_cast<int>(gridDim.y); ++rk)
-        v += cluster.map_shared_rank(part, rk)[slot];
+        v += cluster.map_shared_rank(total, rk)[m * kWarps * rows_cap + rl];
       Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
     }
   }
@@ -290,29 +278,29 @@ template <int MM>
 int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
               const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
               cudaStream_t st) {
-  constexpr int R = MM == 1 ? 4 : 1;
+  constexpr int R = MM <= 2 ? 2 : 1;
   const int G = K / kGroup;
-  auto xs_bytes = [](int gs) {   // fp32 activations + half-group sums of one slice
-    const int b = (gs + kGroupsPerUnit - 1) / kGroupsPerUnit;
-    return static_cast<int64_t>(MM) * b * (512 * 16 + 32 * 4);
-  };
+  // K slices: activations of a slice take MM * 8 KB per 32 groups; split K
+  // only when the whole row does not fit the budget
   int nsplit = 1;
-  while (nsplit < kMaxSplit && xs_bytes((G + nsplit - 1) / nsplit) > kXsBudget) ++nsplit;
+  while (nsplit < kMaxSplit &&
+         static_cast<int64_t>(MM) * (((G + nsplit - 1) / nsplit + 31) / 32) * 8192 > kXsBudget)
+    ++nsplit;
   const int gs = (G + nsplit - 1) / nsplit;
-  if (xs_bytes(gs) > kXsBudget) {
+  if (static_cast<int64_t>(MM) * ((gs + 31) / 32) * 8192 > 200 * 1024) {
     set_error("awq_gemv: K = %d is too large for M = %d (use awq_gemm)", K, MM);
     return AWQ_ERR_SHAPE;
   }
   const int KS = gs * kGroup;
   nsplit = (K + KS - 1) / KS;
-  const int B = (gs + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int B = (gs + 31) / 32;
   const int units = N / R;
-  int gx = num_sms() / nsplit;
+  int gx = 2 * num_sms() / nsplit;
   if (gx > units) gx = units;
   if (gx < 1) gx = 1;
   const int rows_cap = ((units + gx - 1) / gx) * R;
-  const size_t smem = static_cast<size_t>(xs_bytes(gs)) +
-                      static_cast<size_t>(MM) * rows_cap * B * sizeof(float);
+  const size_t smem = static_cast<size_t>(MM) * B * 512 * sizeof(uint4) +
+                      static_cast<size_t>(MM) * kWarps * rows_cap * sizeof(float);
   if (smem > 220 * 1024) {
     set_error("awq_gemv: shared memory plan of %zu bytes too large (N = %d, K = %d, M = %d)",
               smem, N, K, MM);
@@ -329,18 +317,17 @@ int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = nsplit;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = nsplit;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = nsplit > 1 ? 1 : 0;
-  // 2^20 as a run-time value: w * 2^20 >> 32 (= w >> 12) stays a high multiply
-  // on the FMA pipe instead of becoming an integer-pipe shift
-  const uint32_t hi_mult = 1u << 20;
+  cfg.numAttrs = nsplit > 1 ? 2 : 1;
   AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_kernel<MM, R>, X, qweight, scales, zeros, inv_s, N,
-                                  K, KS, rows_cap, hi_mult, Y));
+                                  K, KS, rows_cap, Y));
   return AWQ_OK;
 }
 
