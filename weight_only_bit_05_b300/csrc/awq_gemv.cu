@@ -3,19 +3,22 @@
 // "awq-quantization（AWQ量化技术）Skill" page, section 主要功能和特点: a GEMV kernel
 // serves batch-1 token generation; "AWQ量化实战" §3.4: decoding is bound by the
 // bandwidth of reading the weights.  The kernel streams the packed codes from
-// HBM exactly once and hides the fixed cost of a launch behind that stream:
+// HBM exactly once.  On B300 a single token leaves it bound by the issue rate
+// of the dequantize-and-multiply instructions (about 23 per packed word) on
+// large layers and by the fixed latency of a launch on small ones:
 //
-//  * each CTA owns a balanced range of rows over the whole K; the rows of a
-//    range are contiguous in memory, so before anything else the CTA asks
-//    for its whole range (codes, steps, zero points) to be brought into L2
-//    with bulk prefetches.  The kernel is launched with programmatic stream
-//    serialization, so this starts while the previous kernel on the stream
-//    is still finishing; all loads proper come after griddepcontrol.wait
-//    (and see what that kernel wrote: the prefetch fills only the coherent L2);
+//  * each CTA owns a balanced range of rows over the whole K, one CTA per SM;
+//    the rows of a range are contiguous in memory.  The kernel is launched
+//    with programmatic stream serialization.  Before griddepcontrol.wait a CTA
+//    asks for the head of its range (at most 128 KB of codes, with its steps
+//    and zero points) to be brought into L2 with bulk prefetches.  They fill
+//    only the coherent L2, so they are safe while the previous kernel is still
+//    writing.  The head is bounded because prefetching a whole large layer at
+//    once evicts lines before they are read;
 //  * a lane owns one whole group (16 words = 64 contiguous bytes, one step and
 //    one zero point) of a row per unit; a warp's unit is 32 consecutive groups
-//    of 2 rows, so each activation vector read from shared memory serves two
-//    rows;
+//    of R rows (R = 2 for M <= 2), so each activation vector read from shared
+//    memory serves R rows;
 //  * the scaled activations x~ = fp16(fp32(x) * inv_s) are built once per CTA
 //    into shared memory, interleaved so that the 32 lanes read 32 consecutive
 //    16-byte vectors;
@@ -24,9 +27,18 @@
 //    half of them); HSUB2 of the matching (1024 + z) or (64 + z) gives q - z
 //    exactly, and fma.rn.f32.f16 forms x~ (q - z) exactly in fp32 and adds it
 //    to fp32 accumulators; the group step multiplies each group's sum;
-//  * the 16 warps of a CTA split the CTA's (row pair, group block) units into
-//    contiguous runs, flush a row's sum with warp shuffles into a per-warp
-//    slot, and the slots are added in a fixed order (deterministic);
+//  * the warps of a CTA split the CTA's (row unit, group block) units into
+//    contiguous runs and reduce a row's sum over the lanes with warp
+//    shuffles.  For one or two tokens each warp writes its own slot per row
+//    and the slots are added in warp order; for more tokens a row unit owned
+//    by one warp is written to the CTA's row totals at once and a unit split
+//    between neighbouring warps is finished after one barrier by adding their
+//    partial sums in warp order.  Both are deterministic, and the totals leave
+//    shared memory as coalesced fp16 stores;
+//  * launch shapes: 32 warps (64 registers each) for one or two tokens; 16
+//    warps that take half an SM for the smallest layers, so the next GEMV's
+//    CTA can already sit on the SM and run its prefetch; 16 warps with 128
+//    registers for 3 to 8 tokens, whose accumulators need them;
 //  * only when the activations of the whole K do not fit in shared memory is
 //    K split across the CTAs of a thread-block cluster, whose partial sums
 //    are added in rank order through distributed shared memory.
@@ -39,10 +51,11 @@ namespace cg = cooperative_groups;
 namespace awq {
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSplit = 8;
-constexpr int kXsBudget = 96 * 1024;   // activation bytes per CTA (2 CTAs per SM)
+constexpr size_t kHeadPrefetch = 128 * 1024;   // codes per CTA prefetched into L2 before the wait
+// Layers with at most this many bytes of codes per SM run the 16-warp CTA that
+// leaves room for the next kernel's CTA on the same SM (one or two tokens).
+constexpr size_t kSmallBytesPerSm = 64 * 1024;
 
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t magic) {
   uint32_t d;
@@ -78,24 +91,28 @@ __device__ __forceinline__ void word_dot(uint32_t w, uint32_t zb_even, uint32_t 
   fma_mixed2(d3, x.w, c[2], c[3]);
 }
 
-// Bulk L2 prefetch of [p, p + bytes) in pieces of at most 64 KB, spread over
-// the lanes of the calling warp.
+// Bulk L2 prefetch of [p, p + bytes) in 8 KB pieces spread over the lanes of
+// the calling warp.  The range is widened to 16-byte boundaries; every buffer
+// the kernel reads starts 16-byte aligned and ends on a 16-byte boundary.
 __device__ __forceinline__ void prefetch_range(const void* p, size_t bytes, int lane) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(15);
   const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~static_cast<uintptr_t>(15);
-  constexpr uintptr_t kPiece = 65536;
+  constexpr uintptr_t kPiece = 8192;
   for (uintptr_t a = a0 + lane * kPiece; a < a1; a += 32 * kPiece) {
     const uintptr_t e = a + kPiece < a1 ? a + kPiece : a1;
     prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
   }
 }
 
-template <int MM, int R>
-__global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
+// MM tokens, R rows per unit, kWarps warps per CTA, MINB CTAs per SM for the
+// register budget.
+template <int MM, int R, int kWarps, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB)
     gemv_kernel(const __half* __restrict__ X, const uint32_t* __restrict__ qweight,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros,
                 const float* __restrict__ inv_s, int N, int K, int KS, int rows_cap,
                 __half* __restrict__ Y) {
+  constexpr int kThreads = kWarps * 32;
   extern __shared__ uint4 smem_u4[];
   const int kbeg = blockIdx.y * KS;
   const int klen = min(K - kbeg, KS);          // multiple of 128
@@ -103,7 +120,16 @@ __global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
   const int B = (Gs + 31) / 32;                // group blocks of 32 (one per lane)
   const int gbeg = kbeg / kGroup;
   uint4* xs = smem_u4;                         // [MM][B*16][32]
-  float* red = reinterpret_cast<float*>(xs + static_cast<size_t>(MM) * B * 512);   // [MM][kWarps][rows_cap]
+  // Row sums.  For one or two tokens every warp has its own slot per row,
+  // red[MM][kWarps][rows_cap], added in warp order at the end; for more tokens
+  // (where that table would not fit) a row unit owned by one warp goes to
+  // tot[MM][rows_cap] at once and the units split between warps meet in
+  // part[kWarps][2][R*MM].
+  constexpr bool kSlots = MM <= 2;
+  float* red = reinterpret_cast<float*>(xs + static_cast<size_t>(MM) * B * 512);
+  float* tot = red;
+  float* part = tot + MM * rows_cap;
+  constexpr int kTotStride = kSlots ? kWarps : 1;   // tot[m][rl] sits at red[m][0][rl] then
 
   // rows of this CTA (whole units of R rows, balanced over gridDim.x)
   const int NU = N / R;
@@ -114,12 +140,14 @@ __global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
   const int G = K / kGroup, ZW = (G + 7) / 8, KW = K / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- start streaming this CTA's rows into L2 (before the dependency wait)
-  if (warp == 0) {
-    prefetch_range(qweight + static_cast<size_t>(row_base) * KW, static_cast<size_t>(nrows) * KW * 4, lane);
-  } else if (warp == 1) {
-    prefetch_range(scales + static_cast<size_t>(row_base) * G, static_cast<size_t>(nrows) * G * 2, lane);
-    prefetch_range(zeros + static_cast<size_t>(row_base) * ZW, static_cast<size_t>(nrows) * ZW * 4, lane);
+  // ---- the head of this CTA's rows into L2, before the dependency wait
+  if (warp == 0 && gridDim.y == 1) {
+    const size_t qb = static_cast<size_t>(nrows) * KW * 4;
+    const size_t sb = static_cast<size_t>(nrows) * G * 2;
+    const size_t zb = static_cast<size_t>(nrows) * ZW * 4;
+    prefetch_range(qweight + static_cast<size_t>(row_base) * KW, qb < kHeadPrefetch ? qb : kHeadPrefetch, lane);
+    prefetch_range(scales + static_cast<size_t>(row_base) * G, sb < kHeadPrefetch / 32 ? sb : kHeadPrefetch / 32, lane);
+    prefetch_range(zeros + static_cast<size_t>(row_base) * ZW, zb < kHeadPrefetch / 128 ? zb : kHeadPrefetch / 128, lane);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -154,17 +182,26 @@ __global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
     p = __halves2half2(__float2half_rn(f[3]), __float2half_rn(f[7])); o.w = *reinterpret_cast<uint32_t*>(&p);
     xs[(static_cast<size_t>(m) * B + b) * 512 + j * 32 + l] = o;
   }
-  for (int i = threadIdx.x; i < MM * kWarps * rows_cap; i += kThreads) red[i] = 0.f;
+  if (kSlots)
+    for (int i = threadIdx.x; i < MM * kWarps * rows_cap; i += kThreads) red[i] = 0.f;
   __syncthreads();
 
-  // ---- main loop over this warp's contiguous run of (row unit, group block)
+  // ---- main loop over this warp's contiguous run [ub, ue) of (row unit,
+  // group block) pairs.  Without per-warp slots, a row unit whose blocks all
+  // lie in the run has its total written to tot at once, and the partial sums
+  // of a unit split between neighbouring warps go to part (slot 0: the run's
+  // first row unit, slot 1: its last) and are added after the loop.
+  constexpr int RM = R * MM;
   const int nunits = (u1 - u0) * B;
   const int ub = static_cast<int>(static_cast<int64_t>(warp) * nunits / kWarps);
   const int ue = static_cast<int>(static_cast<int64_t>(warp + 1) * nunits / kWarps);
+  const int ul_first = ub / B;
 
   float acc[R][MM];
   int cur = -1;
   auto flush = [&](int unit_row) {
+    const bool whole = unit_row * B >= ub && (unit_row + 1) * B <= ue;
+    const int slot = unit_row == ul_first ? 0 : 1;
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -172,7 +209,14 @@ __global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
         float v = acc[r][m];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) red[(m * kWarps + warp) * rows_cap + unit_row * R + r] = v;
+        if (lane == 0) {
+          if (kSlots)
+            red[(m * kWarps + warp) * rows_cap + unit_row * R + r] = v;
+          else if (whole)
+            tot[m * rows_cap + unit_row * R + r] = v;
+          else
+            part[(warp * 2 + slot) * RM + r * MM + m] = v;
+        }
       }
   };
 
@@ -234,19 +278,48 @@ __global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
   if (cur >= 0) flush(cur);
   __syncthreads();
 
-  // ---- fixed-order sum of the per-warp slots; cluster reduction over K slices
-  float* total = red;   // warp 0's slots hold the CTA total in the cluster case
-  for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
-    const int m = i / nrows, rl = i - m * nrows;
-    float v = 0.f;
+  if (kSlots) {
+    // fixed-order sum of the per-warp slots into warp 0's slot
+    for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
+      const int m = i / nrows, rl = i - m * nrows;
+      float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) v += red[(m * kWarps + w) * rows_cap + rl];
-    if (gridDim.y == 1)
-      Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
-    else
-      total[m * kWarps * rows_cap + rl] = v;   // only the slot read by this thread changes
+      for (int w = 0; w < kWarps; ++w) v += red[(m * kWarps + w) * rows_cap + rl];
+      if (gridDim.y == 1)
+        Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
+      else
+        red[m * kWarps * rows_cap + rl] = v;   // only the slot read by this thread changes
+    }
+    if (gridDim.y == 1) return;
+  } else {
+    // row units split between warps: the warp in whose run a unit starts
+    // adds its own partial and those of the following warps, in warp order
+    if (ub < ue && lane < RM) {
+      const int ul_last = (ue - 1) / B;
+      if (ul_last * B >= ub && (ul_last + 1) * B > ue) {
+        const int r = lane / MM, m = lane - r * MM;
+        float v = part[(warp * 2 + (ul_last == ul_first ? 0 : 1)) * RM + lane];
+        const int stop = (ul_last + 1) * B;
+        for (int w2 = warp + 1; w2 < kWarps; ++w2) {
+          const int ub2 = static_cast<int>(static_cast<int64_t>(w2) * nunits / kWarps);
+          const int ue2 = static_cast<int>(static_cast<int64_t>(w2 + 1) * nunits / kWarps);
+          if (ub2 >= stop) break;
+          if (ub2 < ue2) v += part[w2 * 2 * RM + lane];
+        }
+        tot[m * rows_cap + ul_last * R + r] = v;
+      }
+    }
+    __syncthreads();
+    if (gridDim.y == 1) {
+      for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
+        const int m = i / nrows, rl = i - m * nrows;
+        Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(tot[m * rows_cap + rl]);
+      }
+      return;
+    }
   }
-  if (gridDim.y == 1) return;
+
+  // ---- K split over a cluster: rank 0 adds the CTA totals in rank order
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   if (cluster.block_rank() == 0) {
@@ -254,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, (MM <= 3 ? 2 : 1))
       const int m = i / nrows, rl = i - m * nrows;
       float v = 0.f;
       for (int rk = 0; rk < static_cast<int>(gridDim.y); ++rk)
-        v += cluster.map_shared_rank(total, rk)[m * kWarps * rows_cap + rl];
+        v += cluster.map_shared_rank(tot, rk)[m * kTotStride * rows_cap + rl];
       Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
     }
   }
@@ -274,11 +347,13 @@ int num_sms() {
   return cached;
 }
 
-template <int MM>
-int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
-              const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
-              cudaStream_t st) {
-  constexpr int R = MM <= 2 ? 2 : 1;
+template <int MM, int R, int kWarps, int MINB>
+int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
+                 const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
+                 cudaStream_t st) {
+  // activation bytes a CTA may hold: a quarter of an SM's shared memory for
+  // the half-SM shape, most of it otherwise
+  constexpr int64_t kXsBudget = MINB == 2 ? 64 * 1024 : 160 * 1024;
   const int G = K / kGroup;
   // K slices: activations of a slice take MM * 8 KB per 32 groups; split K
   // only when the whole row does not fit the budget
@@ -287,34 +362,32 @@ int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
          static_cast<int64_t>(MM) * (((G + nsplit - 1) / nsplit + 31) / 32) * 8192 > kXsBudget)
     ++nsplit;
   const int gs = (G + nsplit - 1) / nsplit;
-  if (static_cast<int64_t>(MM) * ((gs + 31) / 32) * 8192 > 200 * 1024) {
-    set_error("awq_gemv: K = %d is too large for M = %d (use awq_gemm)", K, MM);
-    return AWQ_ERR_SHAPE;
-  }
   const int KS = gs * kGroup;
   nsplit = (K + KS - 1) / KS;
   const int B = (gs + 31) / 32;
   const int units = N / R;
-  int gx = 2 * num_sms() / nsplit;
+  int gx = num_sms() / nsplit;
   if (gx > units) gx = units;
   if (gx < 1) gx = 1;
   const int rows_cap = ((units + gx - 1) / gx) * R;
   const size_t smem = static_cast<size_t>(MM) * B * 512 * sizeof(uint4) +
-                      static_cast<size_t>(MM) * kWarps * rows_cap * sizeof(float);
+                      (MM <= 2 ? static_cast<size_t>(MM) * kWarps * rows_cap * sizeof(float)
+                               : static_cast<size_t>(MM) * rows_cap * sizeof(float) +
+                                     static_cast<size_t>(kWarps) * 2 * R * MM * sizeof(float));
   if (smem > 220 * 1024) {
-    set_error("awq_gemv: shared memory plan of %zu bytes too large (N = %d, K = %d, M = %d)",
-              smem, N, K, MM);
+    set_error("awq_gemv: shared memory plan of %zu bytes too large (N = %d, K = %d, M = %d; "
+              "use awq_gemm)", smem, N, K, MM);
     return AWQ_ERR_SHAPE;
   }
   static bool attr_set = false;
   if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemv_kernel<MM, R>,
+    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemv_kernel<MM, R, kWarps, MINB>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024));
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, nsplit, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -326,9 +399,23 @@ int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = nsplit > 1 ? 2 : 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_kernel<MM, R>, X, qweight, scales, zeros, inv_s, N,
-                                  K, KS, rows_cap, Y));
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_kernel<MM, R, kWarps, MINB>, X, qweight, scales,
+                                  zeros, inv_s, N, K, KS, rows_cap, Y));
   return AWQ_OK;
+}
+
+template <int MM>
+int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
+              const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
+              cudaStream_t st) {
+  if constexpr (MM <= 2) {
+    const size_t code_bytes = static_cast<size_t>(N) * K / 2;
+    if (code_bytes <= kSmallBytesPerSm * num_sms())
+      return launch_shape<MM, 2, 16, 2>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    return launch_shape<MM, 2, 32, 1>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+  } else {
+    return launch_shape<MM, 1, 16, 1>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+  }
 }
 
 }  // namespace
