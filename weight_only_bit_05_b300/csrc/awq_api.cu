@@ -246,8 +246,9 @@ int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16
     AWQ_TRY(launch_prescale(xt, inv_s, M, K, w, st));
     xt = w;
   }
-  return launch_gemm(kGemmOutF16, xt, M, qweight, reinterpret_cast<const __half*>(scales), zeros,
-                     nullptr, N, K, Y, N, nullptr, 0, st);
+  return launch_gemm(kGemmOutF16, xt, inv_s != nullptr, M, qweight,
+                     reinterpret_cast<const __half*>(scales), zeros, nullptr, N, K, Y, N, nullptr,
+                     0, st);
 }
 
 }  // extern "C"

@@ -84,30 +84,51 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   }
 }
 
-// 8 codes of one word -> 8 fp16 weights in natural k order, (q - z) * s.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 zb, __half2 s2) {
-  // magic fp16 pairs 1024 + q: (k0,k4) (k1,k5) (k2,k6) (k3,k7)
-  const uint32_t h0 = (w & 0x000F000Fu) | 0x64006400u;
-  const uint32_t h1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
-  const uint32_t h2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
-  const uint32_t h3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
-  uint32_t p[4];
-  p[0] = __byte_perm(h0, h1, 0x5410);   // (k0, k1)
-  p[1] = __byte_perm(h2, h3, 0x5410);   // (k2, k3)
-  p[2] = __byte_perm(h0, h1, 0x7632);   // (k4, k5)
-  p[3] = __byte_perm(h2, h3, 0x7632);   // (k6, k7)
+// 8 codes of one word -> 8 fp16 weights (q - z) * s.  Magic fp16 numbers:
+// 1024 + q for the even nibbles (bits 0..3 of each 16-bit half) and 64 + q for
+// the odd ones (bits 4..7), so a single shift serves all four pairs; HSUB2 of
+// the matching (1024 + z) or (64 + z) gives q - z exactly and HMUL2 rounds the
+// product to fp16 once.  With PERM the 16 output bytes hold the pairs (k0,k4)
+// (k1,k5) (k2,k6) (k3,k7), the order in which the prescale kernel lays out
+// each 8-element chunk of the activations (a permutation of k applied to both
+// MMA operands leaves every dot product unchanged); otherwise k is natural.
+template <bool PERM>
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t zbe, uint32_t zbo,
+                                              __half2 s2) {
+  const uint32_t t = w >> 8;
+  const uint32_t h0 = (w & 0x000F000Fu) | 0x64006400u;   // (k0, k4)
+  const uint32_t h1 = (w & 0x00F000F0u) | 0x54005400u;   // (k1, k5)
+  const uint32_t h2 = (t & 0x000F000Fu) | 0x64006400u;   // (k2, k6)
+  const uint32_t h3 = (t & 0x00F000F0u) | 0x54005400u;   // (k3, k7)
+  uint32_t p[4], zz[4];
+  if (PERM) {
+    p[0] = h0; p[1] = h1; p[2] = h2; p[3] = h3;
+    zz[0] = zbe; zz[1] = zbo; zz[2] = zbe; zz[3] = zbo;
+  } else {
+    p[0] = __byte_perm(h0, h1, 0x5410);   // (k0, k1)
+    p[1] = __byte_perm(h2, h3, 0x5410);   // (k2, k3)
+    p[2] = __byte_perm(h0, h1, 0x7632);   // (k4, k5)
+    p[3] = __byte_perm(h2, h3, 0x7632);   // (k6, k7)
+    const uint32_t zmix = __byte_perm(zbe, zbo, 0x5410);
+    zz[0] = zmix; zz[1] = zmix; zz[2] = zmix; zz[3] = zmix;
+  }
   uint4 out;
   uint32_t* o = reinterpret_cast<uint32_t*>(&out);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&p[i]), zb);   // q - z, exact
+    const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&p[i]),
+                              *reinterpret_cast<const __half2*>(&zz[i]));   // q - z, exact
     const __half2 v = __hmul2(d, s2);
     o[i] = *reinterpret_cast<const uint32_t*>(&v);
   }
   return out;
 }
 
-template <int BN, int MODE>
+// Steps and zero points run this many groups ahead of the dequantization, so
+// that their global loads never wait on the memory latency.
+constexpr int kSzAhead = 4;
+
+template <int BN, int MODE, bool PERM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_a,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros, int M,
@@ -249,27 +270,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int n = (t % n_tiles) * BM + r;
         const bool row_ok = n < N;
-        // step and zero point of the current group, and of the next one loaded
-        // a group (two stages) ahead so that the global-load latency is hidden
-        __half2 zb = __half2half2(__ushort_as_half(0x6400));
+        // steps and zero points of groups g .. g + kSzAhead - 1, oldest first
+        __half sq[kSzAhead];
+        uint32_t zq[kSzAhead];
+        auto load_sz = [&](int g, __half& sv, uint32_t& zv) {
+          if (row_ok && g < G) {
+            sv = scales[static_cast<size_t>(n) * G + g];
+            zv = (__ldg(zeros + static_cast<size_t>(n) * ZW + (g >> 3)) >> ((g & 7) * 4)) & 15u;
+          } else {
+            sv = __ushort_as_half(0);
+            zv = 0;
+          }
+        };
+#pragma unroll
+        for (int i = 0; i < kSzAhead; ++i) load_sz(i, sq[i], zq[i]);
+        uint32_t zbe = 0x64006400u, zbo = 0x54005400u;
         __half2 s2 = __half2half2(__ushort_as_half(0));
-        __half s_nx = __ushort_as_half(0);
-        uint32_t z_nx = 0;
-        if (row_ok) {
-          s_nx = scales[static_cast<size_t>(n) * G];
-          z_nx = __ldg(zeros + static_cast<size_t>(n) * ZW) & 15u;
-        }
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
           if ((kb * BK) % kGroup == 0) {
             const int g = (kb * BK) / kGroup;
-            s2 = __half2half2(s_nx);
-            zb = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400u | z_nx)));
-            if (row_ok && g + 1 < G) {
-              s_nx = scales[static_cast<size_t>(n) * G + g + 1];
-              z_nx = (__ldg(zeros + static_cast<size_t>(n) * ZW + ((g + 1) >> 3)) >>
-                      (((g + 1) & 7) * 4)) & 15u;
+            s2 = __half2half2(sq[0]);
+            zbe = (0x6400u | zq[0]) * 0x00010001u;          // (1024 + z, 1024 + z)
+            zbo = (0x5400u | (zq[0] << 4)) * 0x00010001u;   // (64 + z, 64 + z)
+#pragma unroll
+            for (int i = 0; i + 1 < kSzAhead; ++i) {
+              sq[i] = sq[i + 1];
+              zq[i] = zq[i + 1];
             }
+            load_sz(g + kSzAhead, sq[kSzAhead - 1], zq[kSzAhead - 1]);
           }
           if (!wait_or_abort(full + s, (it / S) & 1, ab, 4u)) {
             ok = false;
@@ -282,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k
-            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant_word(rw[i], zb, s2);
+            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
+                dequant_word<PERM>(rw[i], zbe, zbo, s2);
           }
           fence_proxy_async_smem();
           mbar_arrive(deq + s);
@@ -336,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// X~ = fp16(fp32(X) * inv_s), written with each 8-element chunk of k in the
+// order (k0,k4) (k1,k5) (k2,k6) (k3,k7) that the dequantization produces.
 __global__ void prescale_kernel(const __half* __restrict__ X, const float* __restrict__ inv_s,
                                 int64_t total8, int K, __half* __restrict__ Xt) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -347,26 +379,24 @@ __global__ void prescale_kernel(const __half* __restrict__ X, const float* __res
   const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
   const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
   const float is[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  const __half2* h = reinterpret_cast<const __half2*>(&xr);
+  const __half* h = reinterpret_cast<const __half*>(&xr);
   uint4 o;
   __half2* oh = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 f = __half22float2(h[j]);
-    oh[j] = __halves2half2(__float2half_rn(__fmul_rn(f.x, is[2 * j])),
-                           __float2half_rn(__fmul_rn(f.y, is[2 * j + 1])));
-  }
+  for (int j = 0; j < 4; ++j)
+    oh[j] = __halves2half2(__float2half_rn(__fmul_rn(__half2float(h[j]), is[j])),
+                           __float2half_rn(__fmul_rn(__half2float(h[j + 4]), is[j + 4])));
   reinterpret_cast<uint4*>(Xt)[i] = o;
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool PERM>
 int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
                 const uint32_t* zeros, int M, int N, int K, void* out, int ldo, const float* yref,
                 int ldy, cudaStream_t st) {
   using C = Cfg<BN, MODE>;
   static bool attr_set = false;
   if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE>,
+    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE, PERM>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr_set = true;
   }
@@ -387,21 +417,21 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE>, tb, ta, scales, zeros, M, N, K, out,
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM>, tb, ta, scales, zeros, M, N, K, out,
                                   ldo, yref, ldy));
   return AWQ_OK;
 }
 
-template <int MODE>
+template <int MODE, bool PERM>
 int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
                 const uint32_t* zeros, int M, int N, int K, void* out, int ldo, const float* yref,
                 int ldy, cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_tile<16, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    case 32: return launch_tile<32, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    case 64: return launch_tile<64, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    case 128: return launch_tile<128, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    default: return launch_tile<256, MODE>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 16: return launch_tile<16, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 32: return launch_tile<32, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 64: return launch_tile<64, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 128: return launch_tile<128, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    default: return launch_tile<256, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
   }
 }
 
@@ -436,9 +466,9 @@ int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __hal
   return AWQ_OK;
 }
 
-int launch_gemm(int mode, const __half* Xt, int M, const uint32_t* qweight, const __half* scales,
-                const uint32_t* zeros, const __half* Wd, int N, int K, void* out, int ldo,
-                const float* yref, int ldy, cudaStream_t st) {
+int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
+                const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
+                void* out, int ldo, const float* yref, int ldy, cudaStream_t st) {
   const int bn = pick_bn(M, mode);
   CUtensorMap tb, ta;
   int rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xt, K, M, static_cast<uint64_t>(K) * 2,
@@ -453,12 +483,21 @@ int launch_gemm(int mode, const __half* Xt, int M, const uint32_t* qweight, cons
   if (rc != AWQ_OK) return rc;
   switch (mode) {
     case kGemmOutF16:
-      return dispatch_bn<kGemmOutF16>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+      if (xt_permuted)
+        return dispatch_bn<kGemmOutF16, true>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
+                                              ldy, st);
+      return dispatch_bn<kGemmOutF16, false>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
+                                             ldy, st);
     case kGemmSqErr:
-      return launch_tile<256, kGemmSqErr>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+      if (!xt_permuted) {
+        set_error("the squared-error matmul takes prescaled activations");
+        return AWQ_ERR_UNSUPPORTED;
+      }
+      return launch_tile<256, kGemmSqErr, true>(tb, ta, scales, zeros, M, N, K, out, ldo, yref,
+                                                ldy, st);
     default:
-      return launch_tile<256, kGemmDenseF32>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy,
-                                             st);
+      return launch_tile<256, kGemmDenseF32, false>(tb, ta, scales, zeros, M, N, K, out, ldo,
+                                                    yref, ldy, st);
   }
 }
 

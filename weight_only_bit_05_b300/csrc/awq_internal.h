@@ -23,16 +23,20 @@ int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* s
 
 // awq_gemm.cu
 enum GemmMode { kGemmOutF16 = 0, kGemmSqErr = 1, kGemmDenseF32 = 2 };
+// Xt = fp16(X * inv_s), each 8-element chunk of k stored as (k0,k4) (k1,k5)
+// (k2,k6) (k3,k7): the layout launch_gemm takes with xt_permuted = true.
 int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
                     cudaStream_t st);
-// Runs the tensor-core kernel on activations `Xt` [M][K] (already scaled).
+// Runs the tensor-core kernel on activations `Xt` [M][K] (already scaled;
+// xt_permuted says whether k is in the prescale kernel's chunk order, which
+// the quantized modes prefer, or natural).
 //   kGemmOutF16  : Y = fp16(Xt * dequant(qweight)^T), out = fp16 [M][ldo]
 //   kGemmSqErr   : out = fp32 partial sums of (Xt*dequant^T - yref)^2 per
 //                  output row, [ceil(M/256)*2][ldo]; yref fp32 [M][ldy]
 //   kGemmDenseF32: out = fp32 Xt * Wd^T, Wd fp16 [N][K] dense
-int launch_gemm(int mode, const __half* Xt, int M, const uint32_t* qweight, const __half* scales,
-                const uint32_t* zeros, const __half* Wd, int N, int K, void* out, int ldo,
-                const float* yref, int ldy, cudaStream_t st);
+int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
+                const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
+                void* out, int ldo, const float* yref, int ldy, cudaStream_t st);
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
 

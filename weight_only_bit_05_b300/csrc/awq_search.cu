@@ -172,13 +172,13 @@ int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32
   for (int r0 = 0; r0 < N; r0 += L.chunk_rows) {
     const int rows = N - r0 < L.chunk_rows ? N - r0 : L.chunk_rows;
     const __half* Wc = Wh + static_cast<size_t>(r0) * K;
-    TRY(launch_gemm(kGemmDenseF32, X, static_cast<int>(T), nullptr, nullptr, nullptr, Wc, rows, K,
-                    yref, rows, nullptr, 0, st));
+    TRY(launch_gemm(kGemmDenseF32, X, false, static_cast<int>(T), nullptr, nullptr, nullptr, Wc,
+                    rows, K, yref, rows, nullptr, 0, st));
     for (int i = 0; i < n_grid; ++i) {
       TRY(launch_pack(Wc, sc_all + static_cast<size_t>(i) * K, rows, K, qw, sc16, zr, st));
       TRY(launch_prescale(X, inv_all + static_cast<size_t>(i) * K, T, K, xt, st));
-      TRY(launch_gemm(kGemmSqErr, xt, static_cast<int>(T), qw, sc16, zr, nullptr, rows, K, part,
-                      rows, yref, rows, st));
+      TRY(launch_gemm(kGemmSqErr, xt, true, static_cast<int>(T), qw, sc16, zr, nullptr, rows, K,
+                      part, rows, yref, rows, st));
       rows_reduce_kernel<<<(rows + 255) / 256, 256, 0, st>>>(
           part, slots, rows, rows, row_err + static_cast<size_t>(i) * N + r0);
       AWQ_CUDA_TRY_LAUNCH("rows_reduce_kernel");
