@@ -41,6 +41,26 @@ MODEL = "llama2-7b"
 SHAPES = ["qkv", "o", "gate_up", "down"]
 PREFILL = [("llama2-7b", s) for s in SHAPES] + [("llama2-13b", s) for s in SHAPES]
 METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofline"
+
+# DRAM bytes (read + write) per launch of the GEMV on each 7B decode shape, from
+# one ncu capture (profiles/gemv_kernel_7b_decode.md).  They are reported only
+# while the kernel source is byte-identical to the one that was captured.
+GEMV_TRAFFIC = {
+    "source": "weight_only_bit_05_b300/csrc/awq_gemv.cu",
+    "sha256": "8c84324af26452933b2224cd963a61787d056ccdd3e321b66c2c240d24d4ed0a",
+    "per_launch": {"qkv": 26216960, "o": 8783360, "gate_up": 46932224, "down": 23538432},
+}
+
+
+def gemv_traffic():
+    """Mean DRAM bytes per GEMV launch over the four shapes (the unit of
+    ``roofline.achieved``), or None when the kernel changed since the capture."""
+    import hashlib
+    with open(os.path.join(ROOT, GEMV_TRAFFIC["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != GEMV_TRAFFIC["sha256"]:
+            return None, None
+    per = GEMV_TRAFFIC["per_launch"]
+    return round(sum(per.values()) / len(per)), dict(per)
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
 
 
@@ -290,6 +310,42 @@ def gemm_prefill(awq, torch, pk, reps=5):
             "per_shape_tflops": out, "includes": "X~ = fp16(X*inv_s) prescale + tcgen05 GEMM"}
 
 
+def gemv_70b(awq, torch, hbm, reps=20):
+    """GB/s of awq_gemv at M = 1 on the four Llama-2-70B shapes: a CUDA graph
+    of launches over enough packed-weight copies that they cannot stay in L2."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    out = {}
+    for name in ("qkv", "o", "gate_up", "down"):
+        K, N, lid = awq_inputs.layer("llama2-70b", name)
+        gen.manual_seed(1000 + lid)
+        qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
+        nbytes = gemv_bytes(1, N, K)
+        ncp = max(4, -(-3 * 126 * 2**20 // nbytes))
+        copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(ncp - 1)]
+        gen.manual_seed(3000 + lid)
+        X = torch.randn((1, K), generator=gen, device=dev).half()
+        inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+        Y = torch.empty((1, N), dtype=torch.float16, device=dev)
+        g = capture(torch, lambda: [awq.gemv(X, q, s_, z, inv_s, out=Y) for q, s_, z in copies])
+        for _ in range(5):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000 / (reps * ncp)
+        gbs = nbytes / us / 1e3
+        out[f"{name} {K}->{N}"] = {"us_per_launch": round(us, 2), "GB/s": round(gbs, 1),
+                                   "frac": round(gbs / hbm, 4), "copies": ncp}
+        del g, copies, qw, sc, zs
+        torch.cuda.empty_cache()
+    return out
+
+
 def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
     """Wall time of awq_search_scales on one layer (20 alphas) and the
     TFLOP/s of its tensor-core work (Y_ref once + 20 squared-error passes)."""
@@ -328,6 +384,7 @@ def main():
     ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-search", action="store_true", help="skip the scale-search timing")
+    ap.add_argument("--no-70b", action="store_true", help="skip the 70B-shape GEMV figures")
     ap.add_argument("--only-gemm", default=None, metavar="MODEL:LAYER:M",
                     help="run only awq_gemm on one shape 3 times (a small case for profilers)")
     args = ap.parse_args()
@@ -466,6 +523,7 @@ def main():
            "path": "pinned host X -> awq.gemv x128 (eager, C ABI) -> pinned host Y"}
 
     gemm = None if args.no_gemm else gemm_prefill(awq, torch, pk)
+    g70 = None if args.no_70b else gemv_70b(awq, torch, hbm)
     search = None if args.no_search else search_run(awq, torch)
     awq.check_device_error()
 
@@ -476,6 +534,7 @@ def main():
         g, dt, threads, desc = oracle_sample(4096, reps=8)
         cpu = {"value": round(g, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": desc + f"; {dt:.1f} s"}
+    traffic, traffic_shape = gemv_traffic()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4),
@@ -488,7 +547,10 @@ def main():
                    "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events",
                    "extra_warmup_steps": extra},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "traffic_per_shape": traffic_shape,
+                     "algorithmic_bytes_per_launch": round(tot_b / len(shapes)),
+                     "frac_of_8tbs_spec": round(achieved / 8000.0, 4),
                      "kernel": "gemv_kernel<1> (awq_gemv)", "peak_kind": pk_kind,
                      "per_shape": per_shape,
                      "bytes_per_launch": {s["name"]: s["bytes"] for s in shapes}},
@@ -496,6 +558,7 @@ def main():
         "gpu_launches": args.steps * len(calls),
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "gemv_70b": g70,
         "gemm_prefill": gemm,
         "search": search,
     }
