@@ -9,4 +9,5 @@ from .awq_oracle import (GROUP, W_BIT, QMAX, N_GRID, TOL_REL, MSE_REL,  # noqa: 
                          pack_codes, unpack_codes, pack_zeros, unpack_zeros,
                          awq_pack, dequant, scaled_activations, linear,
                          ulp_fp16, tolerance, row_errors, search, gram,
-                         row_errors_gram)
+                         row_errors_gram, SILU_LIP, silu, silu_mul_linear,
+                         fold_inv_scales)

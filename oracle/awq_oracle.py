@@ -298,3 +298,60 @@ def row_errors_gram(H, W16, s_c, inv_s, rows=None):
     wq = dequant(qw, sc, zs).astype(np.float64)
     d = wq * np.asarray(inv_s, dtype=np.float64)[None, :] - W16[rows].astype(np.float64)
     return np.einsum("nk,kj,nj->n", d, H, d)
+
+
+# ------------------------------------- fused projections sharing one input
+# [P1] 主要功能和特点 (融合模块加速: fused attention / MLP modules) and [P5]
+# (TinyChat's kernel fusion): the projections that read the same input are
+# one concatenated weight, and the MLP's gate and up projections feed
+# SiLU(gate) * up.  READING: the fused gate/up weight stacks the I gate rows
+# first and the I up rows after them ([2I, K]), and the product is formed from
+# the two projections' exact sums (fp64 here) before the single rounding of
+# the output.
+SILU_LIP = 1.0999   # max |d silu / dx| = 1.09984 (at x = 2.3994), rounded up
+
+
+def silu(x):
+    """``silu(x) = x / (1 + exp(-x))`` in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def silu_mul_linear(X16, qweight, scales, zeros, inv_s=None):
+    """``Y = silu(X~ W^'_gate^T) * (X~ W^'_up^T)`` for a fused [2I, K] weight.
+
+    Returns ``(Y, tol)``: ``Y`` fp64 [M, I] and a per-element tolerance that
+    carries each projection's bound ``e = 4e-3 * sum |x~ w^|`` through the
+    product: ``|d(silu(g) u)| <= L e_g (|u| + e_u) + |silu(g)| e_u`` with
+    ``L`` = :data:`SILU_LIP`, plus 1 fp16 ulp of Y and 1e-6 relative for the
+    fp32 evaluation of silu.
+    """
+    Y2, B2 = linear(X16, qweight, scales, zeros, inv_s)
+    two_i = Y2.shape[1]
+    assert two_i % 2 == 0, "the fused weight has an even number of rows"
+    I = two_i // 2
+    g, u = Y2[:, :I], Y2[:, I:]
+    eg, eu = TOL_REL * B2[:, :I], TOL_REL * B2[:, I:]
+    sg = silu(g)
+    Y = sg * u
+    tol = SILU_LIP * eg * (np.abs(u) + eu) + np.abs(sg) * eu + ulp_fp16(Y) + 1e-6 * np.abs(Y)
+    return Y, tol
+
+
+# ------------------------------- equivalent transformation into the input op
+def fold_inv_scales(W16, inv_s):
+    """Fold ``diag(1/s_c)`` into the operator that produces the layer's input.
+
+    [P5] 工作机制 (等价变换: the salient channels are scaled by an equivalent
+    transformation whose factors come from offline activation statistics):
+    ``(x diag(1/s_c)) (W diag(s_c))^T = x W^T``, so ``1/s_c`` can live in the
+    previous operator instead of a runtime multiply.  ``W16`` holds one row per
+    input channel of the quantized layer: a norm's weight vector ([K] or
+    [K, 1]) or the output rows of the previous linear ([K, C]).  Row k is
+    multiplied by ``inv_s[k]`` in fp32 and rounded to fp16 (RNE).
+    """
+    W = np.asarray(W16, dtype=np.float16)
+    shape = W.shape
+    W2 = W.reshape(shape[0], -1).astype(np.float32)
+    out = (W2 * np.asarray(inv_s, dtype=np.float32)[:, None]).astype(np.float32)
+    return out.astype(np.float16).reshape(shape)
