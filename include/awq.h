@@ -156,6 +156,43 @@ AWQ_API int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight,
              int32_t N, int32_t K, uint16_t* Y, void* workspace,
              size_t ws_bytes, void* stream);
 
+/* ------------------------------------------ fused gate/up (MLP) projection
+ * The two projections of an MLP that read the same input run as one layer
+ * ("awq-quantization" skill page, 主要功能和特点: fused attention/MLP modules;
+ * "什么是激活感知权重量化（AWQ）？": kernel fusion in TinyChat). The weight is the
+ * stack [gate; up] of 2I rows, packed, searched and scaled as one [2I][K]
+ * layer (one s_c for both, since both read the same activations):
+ *   Y[m][j] = fp16( silu(g_mj) * u_mj ),  silu(x) = x / (1 + exp(-x)),
+ * where g_mj and u_mj are the fp32 sums of awq_gemv/awq_gemm for rows j and
+ * I + j, formed in registers without an fp16 rounding in between.
+ * X: fp16 [M][K]; qweight/scales/zeros: [2I] rows of the canonical layout;
+ * inv_s: fp32 [K] or NULL; Y: fp16 [M][I]. I % 4 == 0, K % 128 == 0.
+ * awq_gemv_silu_mul takes 1 <= M <= 8 (CUDA cores, as awq_gemv);
+ * awq_gemm_silu_mul any M >= 1 (tensor cores, as awq_gemm, same workspace
+ * rule: awq_gemm_workspace_size(M, 2I, K) bytes when inv_s is not NULL). */
+AWQ_API int awq_gemv_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
+                      const uint16_t* scales, const uint32_t* zeros,
+                      const float* inv_s, int32_t I, int32_t K, uint16_t* Y,
+                      void* stream);
+AWQ_API int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
+                      const uint16_t* scales, const uint32_t* zeros,
+                      const float* inv_s, int32_t I, int32_t K, uint16_t* Y,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/* ----------------------------- the equivalent transformation, folded offline
+ * ("什么是激活感知权重量化（AWQ）？", 工作机制: salient channels are protected by an
+ * equivalent transformation whose factors come from offline activation
+ * statistics.) (x diag(1/s_c)) (W diag(s_c))^T = x W^T, so 1/s_c can be moved
+ * into the operator that produces x instead of being applied at run time
+ * (then pass inv_s = NULL to the matmuls):
+ *   out[r][c] = fp16( fp32(W[r][c]) * inv_s[r] )   (one rounding, to nearest)
+ * W: fp16 [rows][cols], one row per input channel of the quantized layer: a
+ * norm's weight vector (rows = K, cols = 1) or the output rows of the previous
+ * linear ([K][C]). inv_s: fp32 [rows]. out may equal W (in place).
+ * rows >= 1, cols >= 1. */
+AWQ_API int awq_fold_inv_scales(const uint16_t* W, int64_t rows, int64_t cols,
+                        const float* inv_s, uint16_t* out, void* stream);
+
 /* ------------------------------------------------------------ scale search
  * The activation-aware grid search ("AWQ量化实战" §2.2, §3.3 第四步, §5.1: one
  * coefficient per layer, no backpropagation): a = absmean(X_cal); for each

@@ -97,3 +97,27 @@ def test_stats_and_search_validation():
     bad = list(args)
     bad[10] = None
     assert lib.awq_search_scales(*bad) == AWQ_ERR_NULL
+
+
+def test_fused_gate_up_validation():
+    for f, extra in ((lib.awq_gemv_silu_mul, ()), (lib.awq_gemm_silu_mul, (None, 0))):
+        # I must be a positive multiple of 4 (2I rows, a multiple of 8)
+        assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 6, 512, FAKE, *extra, None) == AWQ_ERR_SHAPE
+        assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 0, 512, FAKE, *extra, None) == AWQ_ERR_SHAPE
+        assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 256, 200, FAKE, *extra, None) == AWQ_ERR_SHAPE
+        assert f(FAKE, 1, None, FAKE, FAKE, None, 256, 512, FAKE, *extra, None) == AWQ_ERR_NULL
+        assert f(FAKE, 1, FAKE, FAKE, FAKE, None, 256, 512, MIS, *extra, None) == AWQ_ERR_ALIGN
+    assert lib.awq_gemv_silu_mul(FAKE, 9, FAKE, FAKE, FAKE, None, 256, 512, FAKE,
+                                 None) == AWQ_ERR_SHAPE
+    # the tensor-core form needs the workspace when inv_s is given
+    assert lib.awq_gemm_silu_mul(FAKE, 4, FAKE, FAKE, FAKE, FAKE, 256, 512, FAKE, None, 0,
+                                 None) == AWQ_ERR_WORKSPACE
+
+
+def test_fold_validation():
+    f = lib.awq_fold_inv_scales
+    assert f(FAKE, 0, 4, FAKE, FAKE, None) == AWQ_ERR_SHAPE
+    assert f(FAKE, 4, 0, FAKE, FAKE, None) == AWQ_ERR_SHAPE
+    assert f(None, 4, 4, FAKE, FAKE, None) == AWQ_ERR_NULL
+    assert f(FAKE, 4, 4, None, FAKE, None) == AWQ_ERR_NULL
+    assert f(FAKE, 4, 4, FAKE, MIS, None) == AWQ_ERR_ALIGN

@@ -27,7 +27,8 @@ import re
 import torch
 
 __all__ = ["lib", "LIB_PATH", "AwqError", "exported_symbols", "absmean", "channel_scales", "pack",
-           "gemv", "gemm", "search", "check_device_error", "gemm_workspace_bytes"]
+           "gemv", "gemm", "search", "check_device_error", "gemm_workspace_bytes",
+           "gemv_silu_mul", "gemm_silu_mul", "fold_inv_scales"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libawq.so")
@@ -57,6 +58,9 @@ _SIGS = {
     "awq_gemv": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p]),
     "awq_gemm_workspace_size": (_sz, [_i32, _i32, _i32]),
     "awq_gemm": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p, _sz, _p]),
+    "awq_gemv_silu_mul": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p]),
+    "awq_gemm_silu_mul": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p, _sz, _p]),
+    "awq_fold_inv_scales": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _p]),
     "awq_search_workspace_size": (_sz, [_i64, _i32, _i32]),
     "awq_search_scales": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p,
                                          _sz, _p, _p, ctypes.POINTER(ctypes.c_int32),
@@ -173,6 +177,40 @@ def gemm(X, qweight, scales, zeros, inv_s=None, out=None, workspace=None):
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.awq_gemm(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N, K,
                         _ptr(Y), _ptr(workspace), nbytes, _stream()))
+    return Y
+
+
+def gemv_silu_mul(X, qweight, scales, zeros, inv_s=None, out=None):
+    """silu(gate) * up for a stacked [gate; up] weight of 2I rows: Y [M][I]."""
+    M, N, K = _linear_args(X, qweight, scales, zeros, inv_s)
+    Y = out if out is not None else torch.empty((M, N // 2), dtype=torch.float16, device=X.device)
+    _check(lib.awq_gemv_silu_mul(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros),
+                                 _ptr(inv_s), N // 2, K, _ptr(Y), _stream()))
+    return Y
+
+
+def gemm_silu_mul(X, qweight, scales, zeros, inv_s=None, out=None, workspace=None):
+    """Tensor-core form of :func:`gemv_silu_mul`, any M."""
+    M, N, K = _linear_args(X, qweight, scales, zeros, inv_s)
+    Y = out if out is not None else torch.empty((M, N // 2), dtype=torch.float16, device=X.device)
+    if inv_s is not None and workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=X.device)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.awq_gemm_silu_mul(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros),
+                                 _ptr(inv_s), N // 2, K, _ptr(Y), _ptr(workspace), nbytes,
+                                 _stream()))
+    return Y
+
+
+def fold_inv_scales(W: torch.Tensor, inv_s: torch.Tensor, out=None):
+    """Row r of W (fp16, one row per input channel: a norm weight [K] or the
+    previous linear's output rows [K][C]) times inv_s[r], rounded to fp16."""
+    _dev(W, torch.float16, "W")
+    _dev(inv_s, torch.float32, "inv_s")
+    rows = W.shape[0]
+    cols = W.numel() // rows if rows else 0
+    Y = out if out is not None else torch.empty_like(W)
+    _check(lib.awq_fold_inv_scales(_ptr(W), rows, cols, _ptr(inv_s), _ptr(Y), _stream()))
     return Y
 
 

@@ -214,15 +214,55 @@ int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16
                      reinterpret_cast<__half*>(Y), static_cast<cudaStream_t>(stream));
 }
 
+int awq_gemv_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
+                      const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
+                      int32_t I, int32_t K, uint16_t* Y, void* stream) {
+  if (I <= 0 || I % 4 != 0) {
+    set_error("awq_gemv_silu_mul: I = %d must be a positive multiple of 4", I);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_kn(2 * I, K));
+  if (M < 1 || M > 8) {
+    set_error("awq_gemv_silu_mul: M = %d must be in [1, 8]", M);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(X, "X"));
+  AWQ_TRY(check_ptr(qweight, "qweight"));
+  AWQ_TRY(check_ptr(scales, "scales"));
+  AWQ_TRY(check_ptr(zeros, "zeros"));
+  AWQ_TRY(check_opt_ptr(inv_s, "inv_s"));
+  AWQ_TRY(check_ptr(Y, "Y"));
+  return launch_gemv(reinterpret_cast<const __half*>(X), M, qweight,
+                     reinterpret_cast<const __half*>(scales), zeros, inv_s, 2 * I, K,
+                     reinterpret_cast<__half*>(Y), static_cast<cudaStream_t>(stream), true);
+}
+
+int awq_fold_inv_scales(const uint16_t* W, int64_t rows, int64_t cols, const float* inv_s,
+                        uint16_t* out, void* stream) {
+  if (rows < 1 || cols < 1) {
+    set_error("awq_fold_inv_scales: rows = %lld and cols = %lld must be >= 1",
+              static_cast<long long>(rows), static_cast<long long>(cols));
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(W, "W"));
+  AWQ_TRY(check_ptr(inv_s, "inv_s"));
+  AWQ_TRY(check_ptr(out, "out"));
+  return launch_fold_inv_scales(reinterpret_cast<const __half*>(W), rows, cols, inv_s,
+                                reinterpret_cast<__half*>(out), static_cast<cudaStream_t>(stream));
+}
+
 size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {
   (void)N;
   if (M <= 0 || K <= 0) return 0;
   return ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256;
 }
 
-int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
-             const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
-             void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+
+int gemm_common(int mode, const uint16_t* X, int32_t M, const uint32_t* qweight,
+                const uint16_t* scales, const uint32_t* zeros, const float* inv_s, int32_t N,
+                int32_t K, uint16_t* Y, int32_t ldy, void* workspace, size_t ws_bytes,
+                void* stream) {
   AWQ_TRY(check_kn(N, K));
   if (M < 1) {
     set_error("awq_gemm: M = %d must be >= 1", M);
@@ -246,9 +286,30 @@ int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16
     AWQ_TRY(launch_prescale(xt, inv_s, M, K, w, st));
     xt = w;
   }
-  return launch_gemm(kGemmOutF16, xt, inv_s != nullptr, M, qweight,
-                     reinterpret_cast<const __half*>(scales), zeros, nullptr, N, K, Y, N, nullptr,
-                     0, st);
+  return launch_gemm(mode, xt, inv_s != nullptr, M, qweight,
+                     reinterpret_cast<const __half*>(scales), zeros, nullptr, N, K, Y, ldy,
+                     nullptr, 0, st);
+}
+
+}  // namespace
+
+int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
+             const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
+             void* workspace, size_t ws_bytes, void* stream) {
+  return gemm_common(kGemmOutF16, X, M, qweight, scales, zeros, inv_s, N, K, Y, N, workspace,
+                     ws_bytes, stream);
+}
+
+int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
+                      const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
+                      int32_t I, int32_t K, uint16_t* Y, void* workspace, size_t ws_bytes,
+                      void* stream) {
+  if (I <= 0 || I % 4 != 0) {
+    set_error("awq_gemm_silu_mul: I = %d must be a positive multiple of 4", I);
+    return AWQ_ERR_SHAPE;
+  }
+  return gemm_common(kGemmSiluF16, X, M, qweight, scales, zeros, inv_s, 2 * I, K, Y, I,
+                     workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

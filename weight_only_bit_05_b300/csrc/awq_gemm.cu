@@ -203,8 +203,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               C::B_BYTES);
           if (MODE == kGemmDenseF32)
             tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
-          else
+          else if (MODE == kGemmSiluF16) {
+            // 64 gate rows and the 64 matching up rows of the tile's pairs
+            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0 / 2);
+            tma_load_2d(sRaw + s * C::RAW_BYTES + (BM / 2) * (BK / 2), &tm_a, full + s,
+                        kb * (BK / 8), N / 2 + n0 / 2);
+          } else {
             tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0);
+          }
           tma_load_2d(sB + s * C::B_BYTES, &tm_b, full + s, kb * BK, m0);
         }
       }
@@ -268,8 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int n = (t % n_tiles) * BM + r;
-        const bool row_ok = n < N;
+        // with the fused gate/up weight, MMA row r of the tile is virtual row
+        // v = n0 + r: gate row v/2 for even v, up row v/2 for odd v
+        const int v = (t % n_tiles) * BM + r;
+        const int n = MODE == kGemmSiluF16 ? (v >> 1) + (v & 1) * (N / 2) : v;
+        const bool row_ok = MODE == kGemmSiluF16 ? (v >> 1) < N / 2 : v < N;
+        const int raw_r = MODE == kGemmSiluF16 ? (r >> 1) + (r & 1) * (BM / 2) : r;
         // steps and zero points of groups g .. g + kSzAhead - 1, oldest first
         __half sq[kSzAhead];
         uint32_t zq[kSzAhead];
@@ -305,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint4 raw =
-              *reinterpret_cast<const uint4*>(sRaw + s * C::RAW_BYTES + r * 32 + half * 16);
+              *reinterpret_cast<const uint4*>(sRaw + s * C::RAW_BYTES + raw_r * 32 + half * 16);
           uint8_t* arow = sA + s * C::A_BYTES + r * 128;
           const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -334,19 +344,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[16];
         tmem_ld16(tmem + b * C::ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
         tmem_ld_wait();
+        if constexpr (MODE == kGemmSiluF16) {
+          // lanes 2i (gate) and 2i + 1 (up) hold one pair: the gate lane
+          // forms silu(gate) * up
+          const int pair = n >> 1;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = m0 + c0 + j;
-          if (m < M && n < N) {
+          for (int j = 0; j < 16; ++j) {
             const float val = __uint_as_float(v[j]);
-            const size_t idx = static_cast<size_t>(m) * ldo + n;
-            if (MODE == kGemmOutF16) {
-              static_cast<__half*>(out)[idx] = __float2half_rn(val);
-            } else if (MODE == kGemmDenseF32) {
-              static_cast<float*>(out)[idx] = val;
-            } else {
-              const float e = val - yref[static_cast<size_t>(m) * ldy + n];
-              sq = fmaf(e, e, sq);
+            const float up = __shfl_xor_sync(0xffffffffu, val, 1);
+            const int m = m0 + c0 + j;
+            if ((lane & 1) == 0 && m < M && pair < N / 2)
+              static_cast<__half*>(out)[static_cast<size_t>(m) * ldo + pair] =
+                  __float2half_rn(val / (1.f + expf(-val)) * up);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < M && n < N) {
+              const float val = __uint_as_float(v[j]);
+              const size_t idx = static_cast<size_t>(m) * ldo + n;
+              if (MODE == kGemmOutF16) {
+                static_cast<__half*>(out)[idx] = __float2half_rn(val);
+              } else if (MODE == kGemmDenseF32) {
+                static_cast<float*>(out)[idx] = val;
+              } else {
+                const float e = val - yref[static_cast<size_t>(m) * ldy + n];
+                sq = fmaf(e, e, sq);
+              }
             }
           }
         }
@@ -436,7 +461,7 @@ int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __ha
 }
 
 int pick_bn(int M, int mode) {
-  if (mode != kGemmOutF16) return 256;
+  if (mode != kGemmOutF16 && mode != kGemmSiluF16) return 256;
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
@@ -474,12 +499,17 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
   int rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xt, K, M, static_cast<uint64_t>(K) * 2,
                         BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != AWQ_OK) return rc;
+  if (mode == kGemmSiluF16 && (N % 2 != 0)) {
+    set_error("the fused gate/up weight needs an even number of rows");
+    return AWQ_ERR_SHAPE;
+  }
   if (mode == kGemmDenseF32)
     rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Wd, K, N,
                       static_cast<uint64_t>(K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, K / 8, N,
-                      static_cast<uint64_t>(K) / 2, BK / 8, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                      static_cast<uint64_t>(K) / 2, BK / 8,
+                      mode == kGemmSiluF16 ? BM / 2 : BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != AWQ_OK) return rc;
   switch (mode) {
     case kGemmOutF16:
@@ -488,6 +518,12 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
                                               ldy, st);
       return dispatch_bn<kGemmOutF16, false>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
                                              ldy, st);
+    case kGemmSiluF16:
+      if (xt_permuted)
+        return dispatch_bn<kGemmSiluF16, true>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
+                                               ldy, st);
+      return dispatch_bn<kGemmSiluF16, false>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
+                                              ldy, st);
     case kGemmSqErr:
       if (!xt_permuted) {
         set_error("the squared-error matmul takes prescaled activations");

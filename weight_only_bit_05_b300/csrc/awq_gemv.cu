@@ -105,8 +105,11 @@ __device__ __forceinline__ void prefetch_range(const void* p, size_t bytes, int 
 }
 
 // MM tokens, R rows per unit, kWarps warps per CTA, MINB CTAs per SM for the
-// register budget.
-template <int MM, int R, int kWarps, int MINB>
+// register budget.  SILU: the weight stacks I gate rows over I up rows and the
+// kernel writes silu(gate) * up ([M][I]); it walks "virtual" rows v in which
+// v = 2j is gate row j and v = 2j + 1 up row j, so a row unit of R = 2 holds
+// one (gate, up) pair and a CTA's range always holds whole pairs.
+template <int MM, int R, int kWarps, int MINB, bool SILU>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     gemv_kernel(const __half* __restrict__ X, const uint32_t* __restrict__ qweight,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros,
@@ -131,23 +134,35 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   float* part = tot + MM * rows_cap;
   constexpr int kTotStride = kSlots ? kWarps : 1;   // tot[m][rl] sits at red[m][0][rl] then
 
-  // rows of this CTA (whole units of R rows, balanced over gridDim.x)
-  const int NU = N / R;
-  const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * NU / gridDim.x);
-  const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * NU / gridDim.x);
-  const int row_base = u0 * R;
+  // rows of this CTA (whole units of R rows, or whole (gate, up) pairs,
+  // balanced over gridDim.x)
+  const int NB = SILU ? N / 2 : N / R;
+  const int per = SILU ? 2 / R : 1;    // row units per balancing unit
+  const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * NB / gridDim.x) * per;
+  const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * NB / gridDim.x) * per;
+  const int row_base = u0 * R;         // first (virtual) row of the CTA
+  const int half_n = N >> 1;
+  // physical row of virtual row v
+  auto phys = [&](int v) { return SILU ? (v >> 1) + (v & 1) * half_n : v; };
   const int nrows = (u1 - u0) * R;
   const int G = K / kGroup, ZW = (G + 7) / 8, KW = K / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- the head of this CTA's rows into L2, before the dependency wait
   if (warp == 0 && gridDim.y == 1) {
-    const size_t qb = static_cast<size_t>(nrows) * KW * 4;
-    const size_t sb = static_cast<size_t>(nrows) * G * 2;
-    const size_t zb = static_cast<size_t>(nrows) * ZW * 4;
-    prefetch_range(qweight + static_cast<size_t>(row_base) * KW, qb < kHeadPrefetch ? qb : kHeadPrefetch, lane);
-    prefetch_range(scales + static_cast<size_t>(row_base) * G, sb < kHeadPrefetch / 32 ? sb : kHeadPrefetch / 32, lane);
-    prefetch_range(zeros + static_cast<size_t>(row_base) * ZW, zb < kHeadPrefetch / 128 ? zb : kHeadPrefetch / 128, lane);
+    // one contiguous physical range, or the gate and the up range
+    constexpr int kRanges = SILU ? 2 : 1;
+    const int prow = SILU ? nrows / 2 : nrows;
+    constexpr size_t cap = kHeadPrefetch / kRanges;
+    for (int h = 0; h < kRanges; ++h) {
+      const size_t r0 = static_cast<size_t>(phys(row_base + h));
+      const size_t qb = static_cast<size_t>(prow) * KW * 4;
+      const size_t sb = static_cast<size_t>(prow) * G * 2;
+      const size_t zb = static_cast<size_t>(prow) * ZW * 4;
+      prefetch_range(qweight + r0 * KW, qb < cap ? qb : cap, lane);
+      prefetch_range(scales + r0 * G, sb < cap / 32 ? sb : cap / 32, lane);
+      prefetch_range(zeros + r0 * ZW, zb < cap / 128 ? zb : cap / 128, lane);
+    }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       uint32_t zbe[R], zbo[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const int row = row_base + ul * R + r;
+        const int row = phys(row_base + ul * R + r);
         const uint4* src = reinterpret_cast<const uint4*>(qweight + static_cast<size_t>(row) * KW + g * 16);
 #pragma unroll
         for (int v = 0; v < 4; ++v) wq[r][v] = __ldg(src + v);
@@ -278,17 +293,32 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   if (cur >= 0) flush(cur);
   __syncthreads();
 
+  // outputs: one per row, or one per (gate, up) pair
+  const int rstep = SILU ? 2 : 1;
+  const int nout = nrows / rstep;
+  const int ld_y = N / rstep;
+  __half* yb = Y + row_base / rstep;
+  auto put = [&](int m, int o, float a, float b) {
+    const float y = SILU ? a / (1.f + expf(-a)) * b : a;
+    yb[static_cast<size_t>(m) * ld_y + o] = __float2half_rn(y);
+  };
+
   if (kSlots) {
     // fixed-order sum of the per-warp slots into warp 0's slot
-    for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
-      const int m = i / nrows, rl = i - m * nrows;
-      float v = 0.f;
+    for (int i = threadIdx.x; i < MM * nout; i += kThreads) {
+      const int m = i / nout, o = i - m * nout;
+      float a = 0.f, b = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += red[(m * kWarps + w) * rows_cap + rl];
-      if (gridDim.y == 1)
-        Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
-      else
-        red[m * kWarps * rows_cap + rl] = v;   // only the slot read by this thread changes
+      for (int w = 0; w < kWarps; ++w) {
+        a += red[(m * kWarps + w) * rows_cap + o * rstep];
+        if (SILU) b += red[(m * kWarps + w) * rows_cap + o * rstep + 1];
+      }
+      if (gridDim.y == 1) {
+        put(m, o, a, b);
+      } else {   // only the slots read by this thread change
+        red[m * kWarps * rows_cap + o * rstep] = a;
+        if (SILU) red[m * kWarps * rows_cap + o * rstep + 1] = b;
+      }
     }
     if (gridDim.y == 1) return;
   } else {
@@ -311,9 +341,9 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     }
     __syncthreads();
     if (gridDim.y == 1) {
-      for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
-        const int m = i / nrows, rl = i - m * nrows;
-        Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(tot[m * rows_cap + rl]);
+      for (int i = threadIdx.x; i < MM * nout; i += kThreads) {
+        const int m = i / nout, o = i - m * nout;
+        put(m, o, tot[m * rows_cap + o * rstep], SILU ? tot[m * rows_cap + o * rstep + 1] : 0.f);
       }
       return;
     }
@@ -323,12 +353,15 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   if (cluster.block_rank() == 0) {
-    for (int i = threadIdx.x; i < MM * nrows; i += kThreads) {
-      const int m = i / nrows, rl = i - m * nrows;
-      float v = 0.f;
-      for (int rk = 0; rk < static_cast<int>(gridDim.y); ++rk)
-        v += cluster.map_shared_rank(tot, rk)[m * kTotStride * rows_cap + rl];
-      Y[static_cast<size_t>(m) * N + row_base + rl] = __float2half_rn(v);
+    for (int i = threadIdx.x; i < MM * nout; i += kThreads) {
+      const int m = i / nout, o = i - m * nout;
+      float a = 0.f, b = 0.f;
+      for (int rk = 0; rk < static_cast<int>(gridDim.y); ++rk) {
+        const float* t = cluster.map_shared_rank(tot, rk) + m * kTotStride * rows_cap + o * rstep;
+        a += t[0];
+        if (SILU) b += t[1];
+      }
+      put(m, o, a, b);
     }
   }
   cluster.sync();   // every CTA's shared memory stays alive until rank 0 has read it
@@ -347,7 +380,7 @@ int num_sms() {
   return cached;
 }
 
-template <int MM, int R, int kWarps, int MINB>
+template <int MM, int R, int kWarps, int MINB, bool SILU>
 int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
                  const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
                  cudaStream_t st) {
@@ -365,11 +398,12 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
   const int KS = gs * kGroup;
   nsplit = (K + KS - 1) / KS;
   const int B = (gs + 31) / 32;
-  const int units = N / R;
+  // balancing units: row units, or (gate, up) pairs
+  const int units = SILU ? N / 2 : N / R;
   int gx = num_sms() / nsplit;
   if (gx > units) gx = units;
   if (gx < 1) gx = 1;
-  const int rows_cap = ((units + gx - 1) / gx) * R;
+  const int rows_cap = ((units + gx - 1) / gx) * (SILU ? 2 : R);
   const size_t smem = static_cast<size_t>(MM) * B * 512 * sizeof(uint4) +
                       (MM <= 2 ? static_cast<size_t>(MM) * kWarps * rows_cap * sizeof(float)
                                : static_cast<size_t>(MM) * rows_cap * sizeof(float) +
@@ -381,7 +415,7 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
   }
   static bool attr_set = false;
   if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemv_kernel<MM, R, kWarps, MINB>,
+    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemv_kernel<MM, R, kWarps, MINB, SILU>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024));
     attr_set = true;
   }
@@ -399,22 +433,38 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = nsplit > 1 ? 2 : 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_kernel<MM, R, kWarps, MINB>, X, qweight, scales,
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_kernel<MM, R, kWarps, MINB, SILU>, X, qweight, scales,
                                   zeros, inv_s, N, K, KS, rows_cap, Y));
   return AWQ_OK;
 }
 
-template <int MM>
+template <int MM, bool SILU>
 int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
               const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
               cudaStream_t st) {
   if constexpr (MM <= 2) {
     const size_t code_bytes = static_cast<size_t>(N) * K / 2;
     if (code_bytes <= kSmallBytesPerSm * num_sms())
-      return launch_shape<MM, 2, 16, 2>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    return launch_shape<MM, 2, 32, 1>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+      return launch_shape<MM, 2, 16, 2, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    return launch_shape<MM, 2, 32, 1, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
   } else {
-    return launch_shape<MM, 1, 16, 1>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    return launch_shape<MM, 1, 16, 1, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+  }
+}
+
+template <bool SILU>
+int launch_m(const __half* X, int M, const uint32_t* qweight, const __half* scales,
+             const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y, cudaStream_t st) {
+  switch (M) {
+    case 1: return launch_mm<1, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 2: return launch_mm<2, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 3: return launch_mm<3, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 4: return launch_mm<4, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 5: return launch_mm<5, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 6: return launch_mm<6, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 7: return launch_mm<7, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 8: return launch_mm<8, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    default: set_error("awq_gemv: M = %d must be in [1, 8]", M); return AWQ_ERR_SHAPE;
   }
 }
 
@@ -422,18 +472,9 @@ int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
 
 int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* scales,
                 const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
-                cudaStream_t st) {
-  switch (M) {
-    case 1: return launch_mm<1>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 2: return launch_mm<2>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 3: return launch_mm<3>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 4: return launch_mm<4>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 5: return launch_mm<5>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 6: return launch_mm<6>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 7: return launch_mm<7>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 8: return launch_mm<8>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    default: set_error("awq_gemv: M = %d must be in [1, 8]", M); return AWQ_ERR_SHAPE;
-  }
+                cudaStream_t st, bool silu_mul) {
+  if (silu_mul) return launch_m<true>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
+  return launch_m<false>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
 }
 
 }  // namespace awq

@@ -17,12 +17,18 @@ int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweig
                 __half* scales, uint32_t* zeros, cudaStream_t st);
 
 // awq_gemv.cu
+// silu_mul: the weight's N rows are I = N/2 gate rows over I up rows and Y
+// receives silu(gate) * up, [M][N/2].
 int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* scales,
                 const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
-                cudaStream_t st);
+                cudaStream_t st, bool silu_mul = false);
+
+// awq_fold.cu
+int launch_fold_inv_scales(const __half* W, int64_t rows, int64_t cols, const float* inv_s,
+                           __half* out, cudaStream_t st);
 
 // awq_gemm.cu
-enum GemmMode { kGemmOutF16 = 0, kGemmSqErr = 1, kGemmDenseF32 = 2 };
+enum GemmMode { kGemmOutF16 = 0, kGemmSqErr = 1, kGemmDenseF32 = 2, kGemmSiluF16 = 3 };
 // Xt = fp16(X * inv_s), each 8-element chunk of k stored as (k0,k4) (k1,k5)
 // (k2,k6) (k3,k7): the layout launch_gemm takes with xt_permuted = true.
 int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
@@ -34,6 +40,8 @@ int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __hal
 //   kGemmSqErr   : out = fp32 partial sums of (Xt*dequant^T - yref)^2 per
 //                  output row, [ceil(M/256)*2][ldo]; yref fp32 [M][ldy]
 //   kGemmDenseF32: out = fp32 Xt * Wd^T, Wd fp16 [N][K] dense
+//   kGemmSiluF16 : the N weight rows stack N/2 gate rows over N/2 up rows;
+//                  out = fp16 silu(gate) * up, [M][ldo] with N/2 columns
 int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
                 const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
                 void* out, int ldo, const float* yref, int ldy, cudaStream_t st);
