@@ -83,100 +83,129 @@ def channel_scales(a: np.ndarray, alpha: float):
 
 
 # --------------------------------------------------- a3: scaled group RTN
-def quantize(W16: np.ndarray, s_c: np.ndarray | None = None):
-    """Asymmetric group round-to-nearest of ``W' = W diag(s_c)``.
+def quantize(W16: np.ndarray, s_c: np.ndarray | None = None, group: int = GROUP,
+             w_bit: int = W_BIT, zero_point: bool = True):
+    """Group round-to-nearest of ``W' = W diag(s_c)``.
 
     [P2] §1.1 (round to nearest), §2.1 (the channel is the input dimension;
     the weight is out x in and is grouped along the input dimension), §2.3
-    (128 consecutive input channels share one step), [P4] (a scale plus a
-    zero point per group), [P1] 步骤 2 (zero_point on, 4 bits, group 128).
+    (``group`` consecutive input channels share one step: 128, also 64 or
+    32), [P4] (a scale plus a zero point per group), [P1] 步骤 2 (zero_point
+    on, 4 bits, group 128), [P2] §3.3 (zero_point off is the symmetric form;
+    8 bits is the conservative width).
 
-    For each row n and group g of 128 input channels (fp32 arithmetic):
+    For each row n and group g (fp32 arithmetic), with qmax = 2^w_bit - 1:
+
+    asymmetric (zero_point on):
       mn, mx = min, max of the group of w'                 (READING: plain)
-      s32    = (mx - mn) / 15, clamped to [2^-14, 65504]   (READING)
+      s32    = (mx - mn) / qmax, clamped to [2^-14, 65504] (READING)
       s      = fp16_rne(s32)            (the stored scale; codes use it)
-      z      = clamp(rint(-mn / s), 0, 15)
-      q      = clamp(rint(w' / s) + z, 0, 15)
+      z      = clamp(rint(-mn / s), 0, qmax)
+      q      = clamp(rint(w' / s) + z, 0, qmax)
+    symmetric (zero_point off), h = 2^(w_bit - 1):
+      s32    = max |w'| / (h - 1), clamped to [2^-14, 65504]
+      q      = clamp(rint(w' / s), -h, h - 1) + h,   z = h
+      READING: [P4] gives the signed range -8..7 for int4; the codes are
+      stored offset by h (unsigned), so the stored zero point is the
+      constant h and dequantization is the same (q - z) * s.
     with ``rint`` = round half to even and IEEE fp32 division.
 
     Returns ``q`` uint8 [N, K], ``z`` uint8 [N, G], ``s16`` float16 [N, G].
     """
+    assert w_bit in (4, 8) and group in (32, 64, 128)
+    qmax = (1 << w_bit) - 1
     W = np.asarray(W16, dtype=np.float16).astype(np.float32)
     N, K = W.shape
-    assert K % GROUP == 0, "K must be a multiple of the group size"
+    assert K % group == 0, "K must be a multiple of the group size"
     if s_c is not None:
         W = (W * np.asarray(s_c, dtype=np.float32)[None, :]).astype(np.float32)
-    G = K // GROUP
-    Wg = W.reshape(N, G, GROUP)
-    mn = Wg.min(axis=2)
-    mx = Wg.max(axis=2)
-    s32 = ((mx - mn) / np.float32(QMAX)).astype(np.float32)
+    G = K // group
+    Wg = W.reshape(N, G, group)
+    if zero_point:
+        mn = Wg.min(axis=2)
+        mx = Wg.max(axis=2)
+        s32 = ((mx - mn) / np.float32(qmax)).astype(np.float32)
+    else:
+        h = 1 << (w_bit - 1)
+        s32 = (np.abs(Wg).max(axis=2) / np.float32(h - 1)).astype(np.float32)
     s32 = np.minimum(np.maximum(s32, S_MIN), S_MAX)
     s16 = s32.astype(np.float16)
     s = s16.astype(np.float32)
-    z = np.clip(np.rint((-mn) / s), 0, QMAX).astype(np.float32)
-    q = np.clip(np.rint(Wg / s[:, :, None]) + z[:, :, None], 0, QMAX)
+    if zero_point:
+        z = np.clip(np.rint((-mn) / s), 0, qmax).astype(np.float32)
+        q = np.clip(np.rint(Wg / s[:, :, None]) + z[:, :, None], 0, qmax)
+    else:
+        z = np.full((N, G), float(h), dtype=np.float32)
+        q = np.clip(np.rint(Wg / s[:, :, None]), -h, h - 1) + h
     return (q.reshape(N, K).astype(np.uint8), z.astype(np.uint8), s16)
 
 
 # ------------------------------------------------------------ packing layout
-def pack_codes(q: np.ndarray) -> np.ndarray:
-    """8 codes per uint32: ``qweight[n, j]`` holds k = 8j+i in bits [4i, 4i+4).
+def pack_codes(q: np.ndarray, w_bit: int = W_BIT) -> np.ndarray:
+    """``32 / w_bit`` codes per uint32: ``qweight[n, j]`` holds k = c j + i in
+    bits [w_bit i, w_bit (i + 1)) with c = 32 / w_bit (8 nibbles or 4 bytes).
 
     [P5] 典型例子 names platform-aware weight packing without fixing a
     layout; this layout is the library's documented canonical one.
     """
+    c = 32 // w_bit
     q = np.asarray(q, dtype=np.uint32)
     N, K = q.shape
-    q = q.reshape(N, K // 8, 8)
-    out = np.zeros((N, K // 8), dtype=np.uint32)
-    for i in range(8):
-        out |= q[:, :, i] << np.uint32(4 * i)
+    q = q.reshape(N, K // c, c)
+    out = np.zeros((N, K // c), dtype=np.uint32)
+    for i in range(c):
+        out |= q[:, :, i] << np.uint32(w_bit * i)
     return out
 
 
-def unpack_codes(qweight: np.ndarray) -> np.ndarray:
+def unpack_codes(qweight: np.ndarray, w_bit: int = W_BIT) -> np.ndarray:
+    c = 32 // w_bit
     qw = np.asarray(qweight, dtype=np.uint32)
     N, J = qw.shape
-    out = np.empty((N, J, 8), dtype=np.uint8)
-    for i in range(8):
-        out[:, :, i] = (qw >> np.uint32(4 * i)) & np.uint32(0xF)
-    return out.reshape(N, J * 8)
+    out = np.empty((N, J, c), dtype=np.uint8)
+    for i in range(c):
+        out[:, :, i] = (qw >> np.uint32(w_bit * i)) & np.uint32((1 << w_bit) - 1)
+    return out.reshape(N, J * c)
 
 
-def pack_zeros(z: np.ndarray) -> np.ndarray:
-    """Zero points, 8 per uint32: group g = 8j+i in nibble i; pad nibbles = 0."""
+def pack_zeros(z: np.ndarray, w_bit: int = W_BIT) -> np.ndarray:
+    """Zero points packed like the codes: group g = c j + i in field i;
+    pad fields = 0."""
+    c = 32 // w_bit
     z = np.asarray(z, dtype=np.uint32)
     N, G = z.shape
-    J = (G + 7) // 8
-    zp = np.zeros((N, J * 8), dtype=np.uint32)
+    J = (G + c - 1) // c
+    zp = np.zeros((N, J * c), dtype=np.uint32)
     zp[:, :G] = z
-    return pack_codes(zp)
+    return pack_codes(zp, w_bit)
 
 
-def unpack_zeros(zeros: np.ndarray, G: int) -> np.ndarray:
-    return unpack_codes(zeros)[:, :G]
+def unpack_zeros(zeros: np.ndarray, G: int, w_bit: int = W_BIT) -> np.ndarray:
+    return unpack_codes(zeros, w_bit)[:, :G]
 
 
-def awq_pack(W16: np.ndarray, s_c: np.ndarray | None = None):
-    """Quantize and pack: returns ``qweight`` uint32 [N, K/8],
-    ``scales`` float16 [N, K/128], ``zeros`` uint32 [N, ceil(G/8)]."""
-    q, z, s16 = quantize(W16, s_c)
-    return pack_codes(q), s16, pack_zeros(z)
+def awq_pack(W16: np.ndarray, s_c: np.ndarray | None = None, group: int = GROUP,
+             w_bit: int = W_BIT, zero_point: bool = True):
+    """Quantize and pack: returns ``qweight`` uint32 [N, K w_bit / 32],
+    ``scales`` float16 [N, K/group], ``zeros`` uint32 [N, ceil(G w_bit / 32)]."""
+    q, z, s16 = quantize(W16, s_c, group, w_bit, zero_point)
+    return pack_codes(q, w_bit), s16, pack_zeros(z, w_bit)
 
 
 # ------------------------------------------------------------ a4: dequant
-def dequant(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray) -> np.ndarray:
-    """``w^' = (q - z) * s`` in fp32 (exact: a 5-bit integer times an fp16).
+def dequant(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+            group: int = GROUP, w_bit: int = W_BIT) -> np.ndarray:
+    """``w^' = (q - z) * s`` in fp32 (exact: a (w_bit+1)-bit integer times an
+    fp16).
 
-    [P4]: the int4 code is mapped back with its group's scale and zero point.
+    [P4]: the integer code is mapped back with its group's scale and zero point.
     """
-    q = unpack_codes(qweight).astype(np.float32)
+    q = unpack_codes(qweight, w_bit).astype(np.float32)
     N, K = q.shape
-    G = K // GROUP
-    z = unpack_zeros(zeros, G).astype(np.float32)
+    G = K // group
+    z = unpack_zeros(zeros, G, w_bit).astype(np.float32)
     s = np.asarray(scales, dtype=np.float16).astype(np.float32)
-    qg = q.reshape(N, G, GROUP)
+    qg = q.reshape(N, G, group)
     return ((qg - z[:, :, None]) * s[:, :, None]).reshape(N, K).astype(np.float32)
 
 
@@ -190,14 +219,14 @@ def scaled_activations(X16: np.ndarray, inv_s: np.ndarray | None) -> np.ndarray:
     return (X * np.asarray(inv_s, dtype=np.float32)[None, :]).astype(np.float32)
 
 
-def linear(X16, qweight, scales, zeros, inv_s=None):
+def linear(X16, qweight, scales, zeros, inv_s=None, group: int = GROUP, w_bit: int = W_BIT):
     """``Y^ = (X diag(1/s_c)) W^'^T`` summed in fp64.
 
     Returns ``(Y, B)``: ``Y`` fp64 [M, N] and the tolerance base
     ``B[m, n] = sum_k |x~_mk * w^'_nk|`` (fp64).
     """
     xt = scaled_activations(X16, inv_s).astype(np.float64)
-    wq = dequant(qweight, scales, zeros).astype(np.float64)
+    wq = dequant(qweight, scales, zeros, group, w_bit).astype(np.float64)
     return xt @ wq.T, np.abs(xt) @ np.abs(wq).T
 
 
@@ -220,7 +249,7 @@ def _reference_output(X16, W16, rows, t0, t1):
     return X @ Wr.T
 
 
-def row_errors(X16, W16, s_c, inv_s, rows=None, token_chunk=4096):
+def row_errors(X16, W16, s_c, inv_s, rows=None, token_chunk=4096, **cfg):
     """Per-output-row squared error ``e_n = sum_t (Y^_tn - Y_tn)^2`` (fp64)
     for the scaled quantization of ``W`` with the given ``s_c``/``inv_s``.
 
@@ -233,8 +262,8 @@ def row_errors(X16, W16, s_c, inv_s, rows=None, token_chunk=4096):
     W16 = np.asarray(W16, dtype=np.float16)
     N = W16.shape[0]
     rows = np.arange(N) if rows is None else np.asarray(rows)
-    qw, sc, zs = awq_pack(W16[rows], s_c)
-    wq = dequant(qw, sc, zs).astype(np.float64)
+    qw, sc, zs = awq_pack(W16[rows], s_c, **cfg)
+    wq = dequant(qw, sc, zs, cfg.get("group", GROUP), cfg.get("w_bit", W_BIT)).astype(np.float64)
     T = X16.shape[0]
     err = np.zeros(len(rows), dtype=np.float64)
     for t0 in range(0, T, token_chunk):
@@ -245,7 +274,7 @@ def row_errors(X16, W16, s_c, inv_s, rows=None, token_chunk=4096):
     return err
 
 
-def search(X16, W16, n_grid: int = N_GRID, rows=None, a=None):
+def search(X16, W16, n_grid: int = N_GRID, rows=None, a=None, **cfg):
     """Activation-aware scale search over ``alpha`` ([P2] §2.2, §3.3 第四步,
     §5.1; [P5] 工作机制: no backpropagation, one coefficient per layer).
 
@@ -267,7 +296,7 @@ def search(X16, W16, n_grid: int = N_GRID, rows=None, a=None):
     row_err = np.zeros((n_grid, len(rows)), dtype=np.float64)
     for i, al in enumerate(alphas):
         s_c, inv_s = channel_scales(a, al)
-        row_err[i] = row_errors(X16, W16, s_c, inv_s, rows)
+        row_err[i] = row_errors(X16, W16, s_c, inv_s, rows, **cfg)
     mse = row_err.sum(axis=1) / (T * len(rows))
     best = int(np.argmin(mse))
     s_c, inv_s = channel_scales(a, alphas[best])
@@ -286,7 +315,7 @@ def gram(X16, token_chunk=4096) -> np.ndarray:
     return H
 
 
-def row_errors_gram(H, W16, s_c, inv_s, rows=None):
+def row_errors_gram(H, W16, s_c, inv_s, rows=None, **cfg):
     """Second route to :func:`row_errors` through the identity
     ``sum_t r_tn^2 = d_n^T H d_n`` with ``d_n = inv_s * w^'_n - w_n`` and
     ``H = X^T X``.  Exact in real arithmetic when ``x~ = x * inv_s``; the
@@ -294,8 +323,8 @@ def row_errors_gram(H, W16, s_c, inv_s, rows=None):
     few 1e-7 relative."""
     W16 = np.asarray(W16, dtype=np.float16)
     rows = np.arange(W16.shape[0]) if rows is None else np.asarray(rows)
-    qw, sc, zs = awq_pack(W16[rows], s_c)
-    wq = dequant(qw, sc, zs).astype(np.float64)
+    qw, sc, zs = awq_pack(W16[rows], s_c, **cfg)
+    wq = dequant(qw, sc, zs, cfg.get("group", GROUP), cfg.get("w_bit", W_BIT)).astype(np.float64)
     d = wq * np.asarray(inv_s, dtype=np.float64)[None, :] - W16[rows].astype(np.float64)
     return np.einsum("nk,kj,nj->n", d, H, d)
 
@@ -317,7 +346,8 @@ def silu(x):
     return x / (1.0 + np.exp(-x))
 
 
-def silu_mul_linear(X16, qweight, scales, zeros, inv_s=None):
+def silu_mul_linear(X16, qweight, scales, zeros, inv_s=None, group: int = GROUP,
+                    w_bit: int = W_BIT):
     """``Y = silu(X~ W^'_gate^T) * (X~ W^'_up^T)`` for a fused [2I, K] weight.
 
     Returns ``(Y, tol)``: ``Y`` fp64 [M, I] and a per-element tolerance that
@@ -326,7 +356,7 @@ def silu_mul_linear(X16, qweight, scales, zeros, inv_s=None):
     ``L`` = :data:`SILU_LIP`, plus 1 fp16 ulp of Y and 1e-6 relative for the
     fp32 evaluation of silu.
     """
-    Y2, B2 = linear(X16, qweight, scales, zeros, inv_s)
+    Y2, B2 = linear(X16, qweight, scales, zeros, inv_s, group, w_bit)
     two_i = Y2.shape[1]
     assert two_i % 2 == 0, "the fused weight has an even number of rows"
     I = two_i // 2
