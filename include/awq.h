@@ -33,7 +33,9 @@
  *     *_workspace_size() function returns.
  *
  * Canonical packed layout (the library's own; the pages only name
- * "platform-aware weight packing", "什么是激活感知权重量化（AWQ）？" 典型例子):
+ * "platform-aware weight packing", "什么是激活感知权重量化（AWQ）？" 典型例子), for the
+ * default configuration (4-bit codes, 128-channel groups; other configurations
+ * at awq_config below):
  *   qweight uint32 [N][K/8]        : word j of row n holds k = 8j+i in bits [4i, 4i+4)
  *   scales  fp16   [N][K/128]      : step of group g of row n
  *   zeros   uint32 [N][ceil(G/8)]  : group g = 8j+i in bits [4i, 4i+4); unused nibbles 0
@@ -65,8 +67,17 @@ extern "C" {
 #define AWQ_ERR_DEVICE      7  /* a kernel reported a bounded wait that ran out */
 
 /* Quantization configuration ("awq-quantization" skill page, 步骤 2: zero_point,
- * q_group_size, w_bit). Only w_bit = 4, group = 128, zero_point = 1 are
- * implemented; n_grid is the number of alpha candidates (1..64, default 20). */
+ * q_group_size, w_bit). w_bit 4 or 8 ("AWQ量化实战" §3.3: 8 bits as the
+ * conservative width), group 128, 64 or 32 (§2.3), zero_point 1 (asymmetric) or
+ * 0 (symmetric, §3.3; "大模型量化部署实战" gives the signed int4 range -8..7);
+ * n_grid is the number of alpha candidates (1..64, default 20).
+ * Packed layout for a configuration (c = 32 / w_bit codes per word, G = K/group):
+ *   qweight uint32 [N][K/c]      : word j of row n holds k = c j + i in bits [w_bit i, w_bit (i+1))
+ *   scales  fp16   [N][G]        : step of group g of row n
+ *   zeros   uint32 [N][ceil(G/c)]: group g = c j + i in field i; unused fields 0
+ * Symmetric codes are stored offset by h = 2^(w_bit-1) (q = clamp(rint(w'/s),
+ * -h, h-1) + h with s = max|w'| / (h-1)), and every zero point is h, so the
+ * matmuls dequantize every configuration as (q - z) * s. */
 typedef struct awq_config {
   int32_t w_bit;
   int32_t group;
@@ -121,11 +132,12 @@ AWQ_API int awq_channel_scales(const float* a, int32_t K, double alpha, float* s
                        float* inv_s, void* stream);
 
 /* ---------------------------------------------------------------- quantizer
- * Scaled group RTN with zero point and packing into the canonical layout
- * ("AWQ量化实战" §1.1, §2.3; "大模型量化部署实战" 核心原理). Codes are decided in
- * fp32 with IEEE division and round-half-even, bit-exact with the definition.
- * W: fp16 [N][K]. s_c: fp32 [K] or NULL (all ones).
- * qweight: uint32 [N][K/8]; scales: fp16 [N][K/128]; zeros: uint32 [N][ceil(G/8)]. */
+ * Scaled group RTN and packing into the canonical layout of the configuration
+ * ("AWQ量化实战" §1.1, §2.3, §3.3; "大模型量化部署实战" 核心原理). Codes are decided
+ * in fp32 with IEEE division and round-half-even, bit-exact with the definition.
+ * W: fp16 [N][K]. s_c: fp32 [K] or NULL (all ones). cfg: NULL = 4/128/1.
+ * Default layout: qweight uint32 [N][K/8]; scales fp16 [N][K/128]; zeros uint32
+ * [N][ceil(G/8)]; other configurations as described at awq_config. */
 AWQ_API int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
              const awq_config* cfg, uint32_t* qweight, uint16_t* scales,
              uint32_t* zeros, void* stream);
@@ -142,6 +154,12 @@ AWQ_API int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight,
              const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
              int32_t N, int32_t K, uint16_t* Y, void* stream);
 
+/* awq_gemv for a configuration's packed layout (cfg NULL = the default 4/128/1;
+ * zero_point does not matter to the matmul, the zero points are stored). */
+AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
+                const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                const float* inv_s, int32_t N, int32_t K, uint16_t* Y, void* stream);
+
 /* ------------------------------------------------------------- GEMM, any M
  * Same result as awq_gemv for any M >= 1, on the 5th-generation tensor cores:
  * packed codes and activations staged by TMA, codes dequantized to fp16 in
@@ -155,6 +173,12 @@ AWQ_API int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight,
              const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
              int32_t N, int32_t K, uint16_t* Y, void* workspace,
              size_t ws_bytes, void* stream);
+/* awq_gemm for a configuration's packed layout (cfg NULL = 4/128/1); the
+ * workspace rule is the same. */
+AWQ_API int awq_gemm_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
+                const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                const float* inv_s, int32_t N, int32_t K, uint16_t* Y, void* workspace,
+                size_t ws_bytes, void* stream);
 
 /* ------------------------------------------ fused gate/up (MLP) projection
  * The two projections of an MLP that read the same input run as one layer

@@ -43,7 +43,7 @@ def assert_linear_close(y_gpu: np.ndarray, X16, qw, sc, zs, inv_s, rows=None, co
     return float((err / tol).max())
 
 
-def row_sq_error_bound(X16, W16, s_c, inv_s, rows, e_ref, token_chunk=4096):
+def row_sq_error_bound(X16, W16, s_c, inv_s, rows, e_ref, token_chunk=4096, **cfg):
     """Rigorous bound on |e_gpu - e_ref| per row for the squared-error pass.
 
     The tensor cores multiply x~ and w^ rounded to fp16 (relative error
@@ -57,8 +57,9 @@ def row_sq_error_bound(X16, W16, s_c, inv_s, rows, e_ref, token_chunk=4096):
     import oracle as O
     W16 = np.asarray(W16, dtype=np.float16)
     K = W16.shape[1]
-    qw, sc, zs = O.awq_pack(W16[rows], s_c)
-    aw = np.abs(O.dequant(qw, sc, zs).astype(np.float64))
+    qw, sc, zs = O.awq_pack(W16[rows], s_c, **cfg)
+    aw = np.abs(O.dequant(qw, sc, zs, cfg.get("group", O.GROUP),
+                          cfg.get("w_bit", O.W_BIT)).astype(np.float64))
     ww = np.abs(W16[rows].astype(np.float64))
     u = 2.0 ** -10 + K * 2.0 ** -23
     D = np.zeros(len(rows))

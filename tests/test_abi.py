@@ -72,7 +72,8 @@ def test_pack_validation_and_config():
     cfg = lib.awq_default_config()
     assert f(FAKE, None, 8, 100, ctypes.byref(cfg), FAKE, FAKE, FAKE, None) == AWQ_ERR_SHAPE
     assert f(FAKE, None, 8, 128, ctypes.byref(cfg), None, FAKE, FAKE, None) == AWQ_ERR_NULL
-    for field, val in (("w_bit", 3), ("group", 64), ("zero_point", 0), ("n_grid", 0)):
+    for field, val in (("w_bit", 3), ("w_bit", 2), ("group", 256), ("group", 96),
+                       ("zero_point", 2), ("n_grid", 0)):
         bad = lib.awq_default_config()
         setattr(bad, field, val)
         assert f(FAKE, None, 8, 128, ctypes.byref(bad), FAKE, FAKE, FAKE, None) == AWQ_ERR_UNSUPPORTED
@@ -121,3 +122,18 @@ def test_fold_validation():
     assert f(None, 4, 4, FAKE, FAKE, None) == AWQ_ERR_NULL
     assert f(FAKE, 4, 4, None, FAKE, None) == AWQ_ERR_NULL
     assert f(FAKE, 4, 4, FAKE, MIS, None) == AWQ_ERR_ALIGN
+
+
+def test_variant_configs_are_accepted_by_validation():
+    # the variants pass configuration checks (and then fail on a later, shape check)
+    f = lib.awq_pack
+    for w_bit, group, zp in ((4, 64, 1), (4, 32, 0), (8, 128, 1), (8, 32, 0)):
+        c = lib.awq_default_config()
+        c.w_bit, c.group, c.zero_point = w_bit, group, zp
+        assert f(FAKE, None, 8, 100, ctypes.byref(c), FAKE, FAKE, FAKE, None) == AWQ_ERR_SHAPE
+        assert lib.awq_gemv_ex(ctypes.byref(c), FAKE, 9, FAKE, FAKE, FAKE, None, 512, 512, FAKE,
+                               None) == AWQ_ERR_SHAPE
+    bad = lib.awq_default_config()
+    bad.w_bit = 3
+    assert lib.awq_gemm_ex(ctypes.byref(bad), FAKE, 4, FAKE, FAKE, FAKE, None, 512, 512, FAKE,
+                           None, 0, None) == AWQ_ERR_UNSUPPORTED

@@ -60,6 +60,10 @@ _SIGS = {
     "awq_gemm": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p, _sz, _p]),
     "awq_gemv_silu_mul": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p]),
     "awq_gemm_silu_mul": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p, _i32, _i32, _p, _p, _sz, _p]),
+    "awq_gemv_ex": (ctypes.c_int, [ctypes.POINTER(AwqConfig), _p, _i32, _p, _p, _p, _p, _i32,
+                                   _i32, _p, _p]),
+    "awq_gemm_ex": (ctypes.c_int, [ctypes.POINTER(AwqConfig), _p, _i32, _p, _p, _p, _p, _i32,
+                                   _i32, _p, _p, _sz, _p]),
     "awq_fold_inv_scales": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _p]),
     "awq_search_workspace_size": (_sz, [_i64, _i32, _i32]),
     "awq_search_scales": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p,
@@ -130,16 +134,24 @@ def channel_scales(a: torch.Tensor, alpha: float):
     return s, inv
 
 
-def pack(W: torch.Tensor, s_c: torch.Tensor | None = None):
+def _cfg(w_bit=4, group=128, zero_point=True, n_grid=20):
+    c = lib.awq_default_config()
+    c.w_bit, c.group, c.zero_point, c.n_grid = w_bit, group, int(bool(zero_point)), n_grid
+    return c
+
+
+def pack(W: torch.Tensor, s_c: torch.Tensor | None = None, w_bit: int = 4, group: int = 128,
+         zero_point: bool = True):
     _dev(W, torch.float16, "W")
     if s_c is not None:
         _dev(s_c, torch.float32, "s_c")
     N, K = W.shape
-    G = K // 128
-    qweight = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    c = 32 // w_bit
+    G = K // group
+    qweight = torch.empty((N, K // c), dtype=torch.int32, device=W.device)
     scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
-    zeros = torch.empty((N, (G + 7) // 8), dtype=torch.int32, device=W.device)
-    cfg = lib.awq_default_config()
+    zeros = torch.empty((N, (G + c - 1) // c), dtype=torch.int32, device=W.device)
+    cfg = _cfg(w_bit, group, zero_point)
     _check(lib.awq_pack(_ptr(W), _ptr(s_c), N, K, ctypes.byref(cfg), _ptr(qweight), _ptr(scales),
                         _ptr(zeros), _stream()))
     return qweight, scales, zeros
@@ -157,11 +169,24 @@ def _linear_args(X, qweight, scales, zeros, inv_s):
     return M, N, K
 
 
+def _layout(K, qweight, scales):
+    """(w_bit, group) of a packed weight, from its shapes."""
+    w_bit = 32 * qweight.shape[1] // K
+    group = K // scales.shape[1]
+    return w_bit, group
+
+
 def gemv(X, qweight, scales, zeros, inv_s=None, out=None):
     M, N, K = _linear_args(X, qweight, scales, zeros, inv_s)
     Y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=X.device)
-    _check(lib.awq_gemv(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N, K,
-                        _ptr(Y), _stream()))
+    w_bit, group = _layout(K, qweight, scales)
+    if (w_bit, group) == (4, 128):
+        _check(lib.awq_gemv(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N,
+                            K, _ptr(Y), _stream()))
+    else:
+        cfg = _cfg(w_bit, group)
+        _check(lib.awq_gemv_ex(ctypes.byref(cfg), _ptr(X), M, _ptr(qweight), _ptr(scales),
+                               _ptr(zeros), _ptr(inv_s), N, K, _ptr(Y), _stream()))
     return Y
 
 
@@ -175,8 +200,15 @@ def gemm(X, qweight, scales, zeros, inv_s=None, out=None, workspace=None):
     if inv_s is not None and workspace is None:
         workspace = torch.empty(gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=X.device)
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib.awq_gemm(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N, K,
-                        _ptr(Y), _ptr(workspace), nbytes, _stream()))
+    w_bit, group = _layout(K, qweight, scales)
+    if (w_bit, group) == (4, 128):
+        _check(lib.awq_gemm(_ptr(X), M, _ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(inv_s), N,
+                            K, _ptr(Y), _ptr(workspace), nbytes, _stream()))
+    else:
+        cfg = _cfg(w_bit, group)
+        _check(lib.awq_gemm_ex(ctypes.byref(cfg), _ptr(X), M, _ptr(qweight), _ptr(scales),
+                               _ptr(zeros), _ptr(inv_s), N, K, _ptr(Y), _ptr(workspace), nbytes,
+                               _stream()))
     return Y
 
 
@@ -214,7 +246,8 @@ def fold_inv_scales(W: torch.Tensor, inv_s: torch.Tensor, out=None):
     return Y
 
 
-def search(X_cal: torch.Tensor, W: torch.Tensor, n_grid: int = 20, row_err: bool = False):
+def search(X_cal: torch.Tensor, W: torch.Tensor, n_grid: int = 20, row_err: bool = False,
+           w_bit: int = 4, group: int = 128, zero_point: bool = True):
     _dev(X_cal, torch.float16, "X_cal")
     _dev(W, torch.float16, "W")
     T, K = X_cal.shape
@@ -225,8 +258,7 @@ def search(X_cal: torch.Tensor, W: torch.Tensor, n_grid: int = 20, row_err: bool
     rerr = torch.empty((n_grid, N), dtype=torch.float64, device=W.device) if row_err else None
     best = ctypes.c_int32(-1)
     mse = (ctypes.c_double * n_grid)()
-    cfg = lib.awq_default_config()
-    cfg.n_grid = n_grid
+    cfg = _cfg(w_bit, group, zero_point, n_grid)
     _check(lib.awq_search_scales(_ptr(X_cal), T, _ptr(W), N, K, ctypes.byref(cfg), _ptr(ws),
                                  ws.numel(), _ptr(s_c), _ptr(inv_s), ctypes.byref(best), mse,
                                  _ptr(rerr), _stream()))

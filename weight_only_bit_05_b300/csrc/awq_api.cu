@@ -100,9 +100,11 @@ int check_opt_ptr(const void* p, const char* name) { return p ? check_ptr(p, nam
 
 int check_cfg(const awq_config* cfg) {
   if (!cfg) return AWQ_OK;  // NULL means the default configuration
-  if (cfg->w_bit != 4 || cfg->group != 128 || cfg->zero_point != 1) {
-    set_error("unsupported configuration w_bit=%d group=%d zero_point=%d (only 4/128/1)",
-              cfg->w_bit, cfg->group, cfg->zero_point);
+  if ((cfg->w_bit != 4 && cfg->w_bit != 8) ||
+      (cfg->group != 128 && cfg->group != 64 && cfg->group != 32) ||
+      (cfg->zero_point != 0 && cfg->zero_point != 1)) {
+    set_error("unsupported configuration w_bit=%d group=%d zero_point=%d (w_bit 4 or 8, "
+              "group 128, 64 or 32, zero_point 0 or 1)", cfg->w_bit, cfg->group, cfg->zero_point);
     return AWQ_ERR_UNSUPPORTED;
   }
   if (cfg->n_grid < 1 || cfg->n_grid > 64) {
@@ -191,13 +193,17 @@ int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K, const aw
   AWQ_TRY(check_ptr(qweight, "qweight"));
   AWQ_TRY(check_ptr(scales, "scales"));
   AWQ_TRY(check_ptr(zeros, "zeros"));
+  const awq_config c = cfg ? *cfg : awq_default_config();
   return launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
-                     reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream));
+                     reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream),
+                     c.w_bit, c.group, c.zero_point != 0);
 }
 
-int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
-             const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
-             void* stream) {
+int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M, const uint32_t* qweight,
+                const uint16_t* scales, const uint32_t* zeros, const float* inv_s, int32_t N,
+                int32_t K, uint16_t* Y, void* stream) {
+  AWQ_TRY(check_cfg(cfg));
+  const awq_config c = cfg ? *cfg : awq_default_config();
   AWQ_TRY(check_kn(N, K));
   if (M < 1 || M > 8) {
     set_error("awq_gemv: M = %d must be in [1, 8]", M);
@@ -211,7 +217,14 @@ int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16
   AWQ_TRY(check_ptr(Y, "Y"));
   return launch_gemv(reinterpret_cast<const __half*>(X), M, qweight,
                      reinterpret_cast<const __half*>(scales), zeros, inv_s, N, K,
-                     reinterpret_cast<__half*>(Y), static_cast<cudaStream_t>(stream));
+                     reinterpret_cast<__half*>(Y), static_cast<cudaStream_t>(stream), false,
+                     c.w_bit, c.group);
+}
+
+int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
+             const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
+             void* stream) {
+  return awq_gemv_ex(nullptr, X, M, qweight, scales, zeros, inv_s, N, K, Y, stream);
 }
 
 int awq_gemv_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
@@ -259,10 +272,12 @@ size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {
 
 namespace {
 
-int gemm_common(int mode, const uint16_t* X, int32_t M, const uint32_t* qweight,
-                const uint16_t* scales, const uint32_t* zeros, const float* inv_s, int32_t N,
-                int32_t K, uint16_t* Y, int32_t ldy, void* workspace, size_t ws_bytes,
-                void* stream) {
+int gemm_common(int mode, const awq_config* cfg, const uint16_t* X, int32_t M,
+                const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
+                const float* inv_s, int32_t N, int32_t K, uint16_t* Y, int32_t ldy,
+                void* workspace, size_t ws_bytes, void* stream) {
+  AWQ_TRY(check_cfg(cfg));
+  const awq_config c = cfg ? *cfg : awq_default_config();
   AWQ_TRY(check_kn(N, K));
   if (M < 1) {
     set_error("awq_gemm: M = %d must be >= 1", M);
@@ -283,12 +298,12 @@ int gemm_common(int mode, const uint16_t* X, int32_t M, const uint32_t* qweight,
       return AWQ_ERR_WORKSPACE;
     }
     __half* w = static_cast<__half*>(workspace);
-    AWQ_TRY(launch_prescale(xt, inv_s, M, K, w, st));
+    AWQ_TRY(launch_prescale(xt, inv_s, M, K, w, st, c.w_bit));
     xt = w;
   }
   return launch_gemm(mode, xt, inv_s != nullptr, M, qweight,
                      reinterpret_cast<const __half*>(scales), zeros, nullptr, N, K, Y, ldy,
-                     nullptr, 0, st);
+                     nullptr, 0, st, c.w_bit, c.group);
 }
 
 }  // namespace
@@ -296,8 +311,15 @@ int gemm_common(int mode, const uint16_t* X, int32_t M, const uint32_t* qweight,
 int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16_t* scales,
              const uint32_t* zeros, const float* inv_s, int32_t N, int32_t K, uint16_t* Y,
              void* workspace, size_t ws_bytes, void* stream) {
-  return gemm_common(kGemmOutF16, X, M, qweight, scales, zeros, inv_s, N, K, Y, N, workspace,
-                     ws_bytes, stream);
+  return gemm_common(kGemmOutF16, nullptr, X, M, qweight, scales, zeros, inv_s, N, K, Y, N,
+                     workspace, ws_bytes, stream);
+}
+
+int awq_gemm_ex(const awq_config* cfg, const uint16_t* X, int32_t M, const uint32_t* qweight,
+                const uint16_t* scales, const uint32_t* zeros, const float* inv_s, int32_t N,
+                int32_t K, uint16_t* Y, void* workspace, size_t ws_bytes, void* stream) {
+  return gemm_common(kGemmOutF16, cfg, X, M, qweight, scales, zeros, inv_s, N, K, Y, N,
+                     workspace, ws_bytes, stream);
 }
 
 int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
@@ -308,7 +330,7 @@ int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
     set_error("awq_gemm_silu_mul: I = %d must be a positive multiple of 4", I);
     return AWQ_ERR_SHAPE;
   }
-  return gemm_common(kGemmSiluF16, X, M, qweight, scales, zeros, inv_s, 2 * I, K, Y, I,
+  return gemm_common(kGemmSiluF16, nullptr, X, M, qweight, scales, zeros, inv_s, 2 * I, K, Y, I,
                      workspace, ws_bytes, stream);
 }
 

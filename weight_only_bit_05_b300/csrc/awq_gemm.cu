@@ -47,11 +47,12 @@ constexpr int kThreads = 64 + 32 * (kDeqWarps + kEpiWarps);
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
-template <int BN, int MODE>
+template <int BN, int MODE, int BITS>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int RAW_BYTES = (MODE == kGemmDenseF32) ? 0 : BM * BK / 2;
+  static constexpr int RAW_ROW = BK * BITS / 8;     // packed bytes of one row per stage
+  static constexpr int RAW_BYTES = (MODE == kGemmDenseF32) ? 0 : BM * RAW_ROW;
   static constexpr int STAGE = A_BYTES + B_BYTES + RAW_BYTES;
   static constexpr int STAGES = (kSmemBudget / STAGE) > 8 ? 8 : (kSmemBudget / STAGE);
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;   // one fp32 accumulator
@@ -124,17 +125,49 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t zbe, uint32_t
   return out;
 }
 
+// Two 8-bit words (codes k0..k7) -> 8 fp16 weights (q - z) * s: bytes 0 and 2
+// of a word (bits 0..7 of each 16-bit half) and, after one shift, bytes 1 and
+// 3 become the fp16 number 1024 + q; HSUB2 and HMUL2 as for 4-bit codes.
+// With PERM the output pairs are (k0,k2) (k1,k3) (k4,k6) (k5,k7), the order of
+// the prescale kernel's 8-bit chunk layout; otherwise k is natural.
+template <bool PERM>
+__device__ __forceinline__ uint4 dequant_word8(uint32_t w0, uint32_t w1, uint32_t zb, __half2 s2) {
+  uint32_t p[4];
+  p[0] = (w0 & 0x00FF00FFu) | 0x64006400u;          // (k0, k2)
+  p[1] = ((w0 >> 8) & 0x00FF00FFu) | 0x64006400u;   // (k1, k3)
+  p[2] = (w1 & 0x00FF00FFu) | 0x64006400u;          // (k4, k6)
+  p[3] = ((w1 >> 8) & 0x00FF00FFu) | 0x64006400u;   // (k5, k7)
+  if (!PERM) {
+    const uint32_t a = p[0], b = p[1], c = p[2], d = p[3];
+    p[0] = __byte_perm(a, b, 0x5410);   // (k0, k1)
+    p[1] = __byte_perm(a, b, 0x7632);   // (k2, k3)
+    p[2] = __byte_perm(c, d, 0x5410);   // (k4, k5)
+    p[3] = __byte_perm(c, d, 0x7632);   // (k6, k7)
+  }
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 dd = __hsub2(*reinterpret_cast<const __half2*>(&p[i]),
+                               *reinterpret_cast<const __half2*>(&zb));   // q - z, exact
+    const __half2 v = __hmul2(dd, s2);
+    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return out;
+}
+
 // Steps and zero points run this many groups ahead of the dequantization, so
 // that their global loads never wait on the memory latency.
 constexpr int kSzAhead = 4;
 
-template <int BN, int MODE, bool PERM>
+template <int BN, int MODE, bool PERM, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_a,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros, int M,
-                int N, int K, void* __restrict__ out, int ldo, const float* __restrict__ yref,
-                int ldy) {
-  using C = Cfg<BN, MODE>;
+                int N, int K, int gs, void* __restrict__ out, int ldo,
+                const float* __restrict__ yref, int ldy) {
+  using C = Cfg<BN, MODE, BITS>;
+  constexpr int KWB = BK * BITS / 32;   // packed words of one row per stage
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -205,11 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
           else if (MODE == kGemmSiluF16) {
             // 64 gate rows and the 64 matching up rows of the tile's pairs
-            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0 / 2);
-            tma_load_2d(sRaw + s * C::RAW_BYTES + (BM / 2) * (BK / 2), &tm_a, full + s,
-                        kb * (BK / 8), N / 2 + n0 / 2);
+            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * KWB, n0 / 2);
+            tma_load_2d(sRaw + s * C::RAW_BYTES + (BM / 2) * C::RAW_ROW, &tm_a, full + s,
+                        kb * KWB, N / 2 + n0 / 2);
           } else {
-            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * (BK / 8), n0);
+            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * KWB, n0);
           }
           tma_load_2d(sB + s * C::B_BYTES, &tm_b, full + s, kb * BK, m0);
         }
@@ -269,8 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (MODE != kGemmDenseF32) {
       const int d = warp - 2;              // 0..7
       const int r = (d & 3) * 32 + lane;   // tile row
-      const int half = d >> 2;             // words 4*half .. 4*half+3 of the stage
-      const int G = K / kGroup, ZW = (G + 7) / 8;
+      const int half = d >> 2;             // input channels 32*half .. +31 of the stage
+      constexpr int PW = 32 / BITS;        // codes per packed word
+      constexpr uint32_t QMASK = (1u << BITS) - 1u;
+      const int G = K / gs, ZW = (G + PW - 1) / PW;
+      // the groups this thread meets, in order: a new one every kb_per_g
+      // stages, gstride groups after the previous one
+      const int kb_per_g = gs >= BK ? gs / BK : 1;
+      const int gstride = gs >= BK ? 1 : BK / gs;
+      const int gfirst = (half * 32) / gs;
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
@@ -280,13 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = MODE == kGemmSiluF16 ? (v >> 1) + (v & 1) * (N / 2) : v;
         const bool row_ok = MODE == kGemmSiluF16 ? (v >> 1) < N / 2 : v < N;
         const int raw_r = MODE == kGemmSiluF16 ? (r >> 1) + (r & 1) * (BM / 2) : r;
-        // steps and zero points of groups g .. g + kSzAhead - 1, oldest first
+        // steps and zero points of this thread's next kSzAhead groups, oldest first
         __half sq[kSzAhead];
         uint32_t zq[kSzAhead];
-        auto load_sz = [&](int g, __half& sv, uint32_t& zv) {
+        auto load_sz = [&](int i, __half& sv, uint32_t& zv) {
+          const int g = gfirst + i * gstride;
           if (row_ok && g < G) {
             sv = scales[static_cast<size_t>(n) * G + g];
-            zv = (__ldg(zeros + static_cast<size_t>(n) * ZW + (g >> 3)) >> ((g & 7) * 4)) & 15u;
+            zv = (__ldg(zeros + static_cast<size_t>(n) * ZW + g / PW) >> ((g % PW) * BITS)) & QMASK;
           } else {
             sv = __ushort_as_half(0);
             zv = 0;
@@ -298,31 +339,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         __half2 s2 = __half2half2(__ushort_as_half(0));
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
-          if ((kb * BK) % kGroup == 0) {
-            const int g = (kb * BK) / kGroup;
+          if (kb % kb_per_g == 0) {
+            const int gi = kb / kb_per_g;   // this thread's group counter
             s2 = __half2half2(sq[0]);
             zbe = (0x6400u | zq[0]) * 0x00010001u;          // (1024 + z, 1024 + z)
-            zbo = (0x5400u | (zq[0] << 4)) * 0x00010001u;   // (64 + z, 64 + z)
+            zbo = (0x5400u | (zq[0] << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
 #pragma unroll
             for (int i = 0; i + 1 < kSzAhead; ++i) {
               sq[i] = sq[i + 1];
               zq[i] = zq[i + 1];
             }
-            load_sz(g + kSzAhead, sq[kSzAhead - 1], zq[kSzAhead - 1]);
+            load_sz(gi + kSzAhead, sq[kSzAhead - 1], zq[kSzAhead - 1]);
           }
           if (!wait_or_abort(full + s, (it / S) & 1, ab, 4u)) {
             ok = false;
             break;
           }
-          const uint4 raw =
-              *reinterpret_cast<const uint4*>(sRaw + s * C::RAW_BYTES + raw_r * 32 + half * 16);
+          const uint8_t* rp = sRaw + s * C::RAW_BYTES + raw_r * C::RAW_ROW + half * (C::RAW_ROW / 2);
           uint8_t* arow = sA + s * C::A_BYTES + r * 128;
-          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          if constexpr (BITS == 4) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(rp);
+            const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k
-            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
-                dequant_word<PERM>(rw[i], zbe, zbo, s2);
+            for (int i = 0; i < 4; ++i) {
+              const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k
+              *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
+                  dequant_word<PERM>(rw[i], zbe, zbo, s2);
+            }
+          } else {
+            const uint4 r0 = *reinterpret_cast<const uint4*>(rp);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(rp + 16);
+            const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = half * 4 + i;   // 16-byte chunk = 8 consecutive k = 2 words
+              *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
+                  dequant_word8<PERM>(rw[2 * i], rw[2 * i + 1], zbe, s2);
+            }
           }
           fence_proxy_async_smem();
           mbar_arrive(deq + s);
@@ -345,17 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + b * C::ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
         tmem_ld_wait();
         if constexpr (MODE == kGemmSiluF16) {
-          // lanes 2i (gate) and 2i + 1 (up) hold one pair: the gate lane
-          // forms silu(gate) * up
+          // lanes 2i (gate) and 2i + 1 (up) hold one pair for 16 tokens; per
+          // two tokens the gate lane finishes the first and the up lane the
+          // second, after one exchange
           const int pair = n >> 1;
+          const bool gate_lane = (lane & 1) == 0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float val = __uint_as_float(v[j]);
-            const float up = __shfl_xor_sync(0xffffffffu, val, 1);
-            const int m = m0 + c0 + j;
-            if ((lane & 1) == 0 && m < M && pair < N / 2)
+          for (int j = 0; j < 16; j += 2) {
+            const float a0 = __uint_as_float(v[j]), a1 = __uint_as_float(v[j + 1]);
+            const float got = __shfl_xor_sync(0xffffffffu, gate_lane ? a1 : a0, 1);
+            const float g = gate_lane ? a0 : got, u = gate_lane ? got : a1;
+            const int m = m0 + c0 + j + (gate_lane ? 0 : 1);
+            if (m < M && pair < N / 2)
               static_cast<__half*>(out)[static_cast<size_t>(m) * ldo + pair] =
-                  __float2half_rn(val / (1.f + expf(-val)) * up);
+                  __float2half_rn(g / (1.f + expf(-g)) * u);
           }
         } else {
 #pragma unroll
@@ -392,7 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // X~ = fp16(fp32(X) * inv_s), written with each 8-element chunk of k in the
-// order (k0,k4) (k1,k5) (k2,k6) (k3,k7) that the dequantization produces.
+// pair order the dequantization produces: (k0,k4) (k1,k5) (k2,k6) (k3,k7) for
+// 4-bit codes, (k0,k2) (k1,k3) (k4,k6) (k5,k7) for 8-bit codes.
+template <int BITS>
 __global__ void prescale_kernel(const __half* __restrict__ X, const float* __restrict__ inv_s,
                                 int64_t total8, int K, __half* __restrict__ Xt) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -407,21 +465,25 @@ __global__ void prescale_kernel(const __half* __restrict__ X, const float* __res
   const __half* h = reinterpret_cast<const __half*>(&xr);
   uint4 o;
   __half2* oh = reinterpret_cast<__half2*>(&o);
+  constexpr int lo[4] = {0, 1, BITS == 4 ? 2 : 4, BITS == 4 ? 3 : 5};
+  constexpr int step = BITS == 4 ? 4 : 2;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    oh[j] = __halves2half2(__float2half_rn(__fmul_rn(__half2float(h[j]), is[j])),
-                           __float2half_rn(__fmul_rn(__half2float(h[j + 4]), is[j + 4])));
+  for (int j = 0; j < 4; ++j) {
+    const int a0 = lo[j], a1 = lo[j] + step;
+    oh[j] = __halves2half2(__float2half_rn(__fmul_rn(__half2float(h[a0]), is[a0])),
+                           __float2half_rn(__fmul_rn(__half2float(h[a1]), is[a1])));
+  }
   reinterpret_cast<uint4*>(Xt)[i] = o;
 }
 
-template <int BN, int MODE, bool PERM>
+template <int BN, int MODE, bool PERM, int BITS>
 int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
-                const uint32_t* zeros, int M, int N, int K, void* out, int ldo, const float* yref,
-                int ldy, cudaStream_t st) {
-  using C = Cfg<BN, MODE>;
+                const uint32_t* zeros, int M, int N, int K, int gs, void* out, int ldo,
+                const float* yref, int ldy, cudaStream_t st) {
+  using C = Cfg<BN, MODE, BITS>;
   static bool attr_set = false;
   if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE, PERM>,
+    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE, PERM, BITS>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr_set = true;
   }
@@ -442,21 +504,31 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM>, tb, ta, scales, zeros, M, N, K, out,
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM, BITS>, tb, ta, scales, zeros, M, N, K, gs, out,
                                   ldo, yref, ldy));
   return AWQ_OK;
 }
 
-template <int MODE, bool PERM>
+template <int MODE, bool PERM, int BITS>
 int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
-                const uint32_t* zeros, int M, int N, int K, void* out, int ldo, const float* yref,
-                int ldy, cudaStream_t st) {
+                const uint32_t* zeros, int M, int N, int K, int gs, void* out, int ldo,
+                const float* yref, int ldy, cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_tile<16, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    case 32: return launch_tile<32, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    case 64: return launch_tile<64, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    case 128: return launch_tile<128, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
-    default: return launch_tile<256, MODE, PERM>(tb, ta, scales, zeros, M, N, K, out, ldo, yref, ldy, st);
+    case 16:
+      return launch_tile<16, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
+                                               ldy, st);
+    case 32:
+      return launch_tile<32, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
+                                               ldy, st);
+    case 64:
+      return launch_tile<64, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
+                                               ldy, st);
+    case 128:
+      return launch_tile<128, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
+                                                yref, ldy, st);
+    default:
+      return launch_tile<256, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
+                                                yref, ldy, st);
   }
 }
 
@@ -474,7 +546,7 @@ int pick_bn(int M, int mode) {
 int gemm_sqerr_slots(int M) { return (M + 255) / 256; }
 
 int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
-                    cudaStream_t st) {
+                    cudaStream_t st, int w_bit) {
   const int64_t total8 = M * K / 8;
   const int threads = 256;
   const int64_t blocks = (total8 + threads - 1) / threads;
@@ -487,13 +559,60 @@ int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __hal
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, prescale_kernel, X, inv_s, total8, K, Xt));
+  if (w_bit == 8)
+    AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, prescale_kernel<8>, X, inv_s, total8, K, Xt));
+  else
+    AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, prescale_kernel<4>, X, inv_s, total8, K, Xt));
   return AWQ_OK;
 }
 
+namespace {
+
+template <int BITS>
+int launch_gemm_bits(int mode, int bn, const CUtensorMap& tb, const CUtensorMap& ta,
+                     bool xt_permuted, int M, const __half* scales, const uint32_t* zeros, int N,
+                     int K, int gs, void* out, int ldo, const float* yref, int ldy,
+                     cudaStream_t st) {
+  switch (mode) {
+    case kGemmOutF16:
+      if (xt_permuted)
+        return dispatch_bn<kGemmOutF16, true, BITS>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
+                                                    ldo, yref, ldy, st);
+      return dispatch_bn<kGemmOutF16, false, BITS>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
+                                                   ldo, yref, ldy, st);
+    case kGemmSiluF16:
+      if constexpr (BITS == 4) {
+        if (xt_permuted)
+          return dispatch_bn<kGemmSiluF16, true, 4>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
+                                                    ldo, yref, ldy, st);
+        return dispatch_bn<kGemmSiluF16, false, 4>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
+                                                   ldo, yref, ldy, st);
+      }
+      set_error("the fused gate/up layer takes 4-bit codes");
+      return AWQ_ERR_UNSUPPORTED;
+    case kGemmSqErr:
+      if (!xt_permuted) {
+        set_error("the squared-error matmul takes prescaled activations");
+        return AWQ_ERR_UNSUPPORTED;
+      }
+      return launch_tile<256, kGemmSqErr, true, BITS>(tb, ta, scales, zeros, M, N, K, gs, out,
+                                                      ldo, yref, ldy, st);
+    default:
+      return launch_tile<256, kGemmDenseF32, false, 4>(tb, ta, scales, zeros, M, N, K, gs, out,
+                                                       ldo, yref, ldy, st);
+  }
+}
+
+}  // namespace
+
 int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
                 const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
-                void* out, int ldo, const float* yref, int ldy, cudaStream_t st) {
+                void* out, int ldo, const float* yref, int ldy, cudaStream_t st, int w_bit,
+                int group) {
+  if ((w_bit != 4 && w_bit != 8) || (group != 32 && group != 64 && group != 128)) {
+    set_error("awq_gemm: w_bit = %d, group = %d is not supported", w_bit, group);
+    return AWQ_ERR_UNSUPPORTED;
+  }
   const int bn = pick_bn(M, mode);
   CUtensorMap tb, ta;
   int rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xt, K, M, static_cast<uint64_t>(K) * 2,
@@ -503,38 +622,21 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
     set_error("the fused gate/up weight needs an even number of rows");
     return AWQ_ERR_SHAPE;
   }
-  if (mode == kGemmDenseF32)
+  if (mode == kGemmDenseF32) {
     rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Wd, K, N,
                       static_cast<uint64_t>(K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
-  else
-    rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, K / 8, N,
-                      static_cast<uint64_t>(K) / 2, BK / 8,
+  } else {
+    const int pw = 32 / w_bit;   // codes per packed word
+    rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, K / pw, N,
+                      static_cast<uint64_t>(K / pw) * 4, BK / pw,
                       mode == kGemmSiluF16 ? BM / 2 : BM, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (rc != AWQ_OK) return rc;
-  switch (mode) {
-    case kGemmOutF16:
-      if (xt_permuted)
-        return dispatch_bn<kGemmOutF16, true>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
-                                              ldy, st);
-      return dispatch_bn<kGemmOutF16, false>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
-                                             ldy, st);
-    case kGemmSiluF16:
-      if (xt_permuted)
-        return dispatch_bn<kGemmSiluF16, true>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
-                                               ldy, st);
-      return dispatch_bn<kGemmSiluF16, false>(bn, tb, ta, scales, zeros, M, N, K, out, ldo, yref,
-                                              ldy, st);
-    case kGemmSqErr:
-      if (!xt_permuted) {
-        set_error("the squared-error matmul takes prescaled activations");
-        return AWQ_ERR_UNSUPPORTED;
-      }
-      return launch_tile<256, kGemmSqErr, true>(tb, ta, scales, zeros, M, N, K, out, ldo, yref,
-                                                ldy, st);
-    default:
-      return launch_tile<256, kGemmDenseF32, false>(tb, ta, scales, zeros, M, N, K, out, ldo,
-                                                    yref, ldy, st);
   }
+  if (rc != AWQ_OK) return rc;
+  if (w_bit == 8)
+    return launch_gemm_bits<8>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
+                               ldo, yref, ldy, st);
+  return launch_gemm_bits<4>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
+                             ldo, yref, ldy, st);
 }
 
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags) {

@@ -91,6 +91,17 @@ __device__ __forceinline__ void word_dot(uint32_t w, uint32_t zb_even, uint32_t 
   fma_mixed2(d3, x.w, c[2], c[3]);
 }
 
+// x~ (q - z) for the 4 codes of one 8-bit word into four fp32 accumulators:
+// bytes 0 and 2 (bits 0..7 of each half) and bytes 1 and 3 become 1024 + q;
+// xa holds the activations (k0, k2), xb (k1, k3).
+__device__ __forceinline__ void word_dot8(uint32_t w, uint32_t zb, uint32_t xa, uint32_t xb,
+                                          float (&c)[4]) {
+  const uint32_t d0 = hsub2_u(and_or(w, 0x00FF00FFu, 0x64006400u), zb);        // (k0, k2)
+  const uint32_t d1 = hsub2_u(and_or(w >> 8, 0x00FF00FFu, 0x64006400u), zb);   // (k1, k3)
+  fma_mixed2(d0, xa, c[0], c[1]);
+  fma_mixed2(d1, xb, c[2], c[3]);
+}
+
 // Bulk L2 prefetch of [p, p + bytes) in 8 KB pieces spread over the lanes of
 // the calling warp.  The range is widened to 16-byte boundaries; every buffer
 // the kernel reads starts 16-byte aligned and ends on a 16-byte boundary.
@@ -109,27 +120,38 @@ __device__ __forceinline__ void prefetch_range(const void* p, size_t bytes, int 
 // kernel writes silu(gate) * up ([M][I]); it walks "virtual" rows v in which
 // v = 2j is gate row j and v = 2j + 1 up row j, so a row unit of R = 2 holds
 // one (gate, up) pair and a CTA's range always holds whole pairs.
-template <int MM, int R, int kWarps, int MINB, bool SILU>
+// BITS-bit codes (4 or 8) with GS-channel groups (128, 64 or 32): a lane
+// chunk is always 16 packed words (128 channels of 4-bit codes, 64 of 8-bit);
+// groups smaller than a chunk are segments with their own step and zero
+// point, folded into the row sum as each segment ends.
+template <int MM, int R, int kWarps, int MINB, bool SILU, int BITS, int GS>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     gemv_kernel(const __half* __restrict__ X, const uint32_t* __restrict__ qweight,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros,
                 const float* __restrict__ inv_s, int N, int K, int KS, int rows_cap,
                 __half* __restrict__ Y) {
   constexpr int kThreads = kWarps * 32;
+  constexpr int CK = BITS == 4 ? 128 : 64;      // input channels per lane chunk
+  constexpr int OCT = CK / 8;                   // x~ vectors (8 channels) per chunk
+  constexpr int XB = 32 * OCT;                  // x~ vectors per block of 32 chunks
+  constexpr int NSEG = CK > GS ? CK / GS : 1;   // groups per chunk
+  constexpr int SEGW = 16 / NSEG;               // packed words per group segment
+  constexpr int PW = 32 / BITS;                 // codes per packed word
+  constexpr uint32_t QMASK = (1u << BITS) - 1u;
   extern __shared__ uint4 smem_u4[];
   const int kbeg = blockIdx.y * KS;
   const int klen = min(K - kbeg, KS);          // multiple of 128
-  const int Gs = klen / kGroup;                // groups in the slice
-  const int B = (Gs + 31) / 32;                // group blocks of 32 (one per lane)
-  const int gbeg = kbeg / kGroup;
-  uint4* xs = smem_u4;                         // [MM][B*16][32]
+  const int Cs = klen / CK;                    // lane chunks in the slice
+  const int B = (Cs + 31) / 32;                // chunk blocks of 32 (one chunk per lane)
+  const int cbeg = kbeg / CK;
+  uint4* xs = smem_u4;                         // [MM][B][OCT][32]
   // Row sums.  For one or two tokens every warp has its own slot per row,
   // red[MM][kWarps][rows_cap], added in warp order at the end; for more tokens
   // (where that table would not fit) a row unit owned by one warp goes to
   // tot[MM][rows_cap] at once and the units split between warps meet in
   // part[kWarps][2][R*MM].
   constexpr bool kSlots = MM <= 2;
-  float* red = reinterpret_cast<float*>(xs + static_cast<size_t>(MM) * B * 512);
+  float* red = reinterpret_cast<float*>(xs + static_cast<size_t>(MM) * B * XB);
   float* tot = red;
   float* part = tot + MM * rows_cap;
   constexpr int kTotStride = kSlots ? kWarps : 1;   // tot[m][rl] sits at red[m][0][rl] then
@@ -145,7 +167,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // physical row of virtual row v
   auto phys = [&](int v) { return SILU ? (v >> 1) + (v & 1) * half_n : v; };
   const int nrows = (u1 - u0) * R;
-  const int G = K / kGroup, ZW = (G + 7) / 8, KW = K / 8;
+  const int G = K / GS, ZW = (G + PW - 1) / PW, KW = K / PW;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- the head of this CTA's rows into L2, before the dependency wait
@@ -167,11 +189,14 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
-  // ---- prologue: x~ into shared memory, zero the per-warp row slots
-  const int nw = klen / 8;   // packed words per row in the slice
-  for (int idx = threadIdx.x; idx < MM * nw; idx += kThreads) {
-    const int m = idx / nw, c = idx - m * nw;
-    const int gl = c >> 4, j = c & 15, b = gl >> 5, l = gl & 31;
+  // ---- prologue: x~ into shared memory, zero the per-warp row slots.  An
+  // 8-channel vector holds the fp16 pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) for
+  // 4-bit codes (one packed word) and (k0,k2) (k1,k3) (k4,k6) (k5,k7) for
+  // 8-bit codes (two packed words), the pairs the dequantization produces.
+  const int n8 = klen / 8;   // 8-channel vectors per row in the slice
+  for (int idx = threadIdx.x; idx < MM * n8; idx += kThreads) {
+    const int m = idx / n8, c = idx - m * n8;
+    const int cl = c / OCT, o = c - cl * OCT, b = cl >> 5, l = cl & 31;
     const size_t xo = static_cast<size_t>(m) * K + kbeg + 8 * c;
     const uint4 xr = __ldg(reinterpret_cast<const uint4*>(X + xo));
     const __half2* xh = reinterpret_cast<const __half2*>(&xr);
@@ -189,13 +214,17 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
 #pragma unroll
       for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], is[i]);
     }
-    uint4 o;
-    __half2 p;
-    p = __halves2half2(__float2half_rn(f[0]), __float2half_rn(f[4])); o.x = *reinterpret_cast<uint32_t*>(&p);
-    p = __halves2half2(__float2half_rn(f[1]), __float2half_rn(f[5])); o.y = *reinterpret_cast<uint32_t*>(&p);
-    p = __halves2half2(__float2half_rn(f[2]), __float2half_rn(f[6])); o.z = *reinterpret_cast<uint32_t*>(&p);
-    p = __halves2half2(__float2half_rn(f[3]), __float2half_rn(f[7])); o.w = *reinterpret_cast<uint32_t*>(&p);
-    xs[(static_cast<size_t>(m) * B + b) * 512 + j * 32 + l] = o;
+    // pair partners: i and i + 4 (4-bit), or within each half i and i + 2
+    constexpr int lo[4] = {0, 1, BITS == 4 ? 2 : 4, BITS == 4 ? 3 : 5};
+    constexpr int step = BITS == 4 ? 4 : 2;
+    uint4 o4;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 p = __halves2half2(__float2half_rn(f[lo[i]]), __float2half_rn(f[lo[i] + step]));
+      ow[i] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    xs[(static_cast<size_t>(m) * B + b) * XB + o * 32 + l] = o4;
   }
   if (kSlots)
     for (int i = threadIdx.x; i < MM * kWarps * rows_cap; i += kThreads) red[i] = 0.f;
@@ -245,49 +274,80 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
 #pragma unroll
         for (int m = 0; m < MM; ++m) acc[r][m] = 0.f;
     }
-    const int gl = b * 32 + lane;
-    if (gl < Gs) {
-      const int g = gbeg + gl;
+    const int cl = b * 32 + lane;
+    if (cl < Cs) {
+      const int c = cbeg + cl;                  // chunk index in the row
+      const int g0 = c * CK / GS;               // group of the chunk's first segment
       uint4 wq[R][4];
-      float s[R];
-      uint32_t zbe[R], zbo[R];
+      float s[R][NSEG];
+      uint32_t zbe[R][NSEG], zbo[R][NSEG];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int row = phys(row_base + ul * R + r);
-        const uint4* src = reinterpret_cast<const uint4*>(qweight + static_cast<size_t>(row) * KW + g * 16);
+        const uint4* src = reinterpret_cast<const uint4*>(qweight + static_cast<size_t>(row) * KW + c * 16);
 #pragma unroll
         for (int v = 0; v < 4; ++v) wq[r][v] = __ldg(src + v);
-        s[r] = __half2float(scales[static_cast<size_t>(row) * G + g]);
-        const uint32_t z = (__ldg(zeros + static_cast<size_t>(row) * ZW + (g >> 3)) >> ((g & 7) * 4)) & 15u;
-        zbe[r] = (0x6400u | z) * 0x00010001u;          // (1024 + z, 1024 + z)
-        zbo[r] = (0x5400u | (z << 4)) * 0x00010001u;   // (64 + z, 64 + z)
-      }
-      float c[R][MM][4];
 #pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int m = 0; m < MM; ++m)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) c[r][m][i] = 0.f;
-      const uint4* xp = xs + static_cast<size_t>(b) * 512 + lane;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-#pragma unroll
-        for (int m = 0; m < MM; ++m) {
-          const uint4 xv = xp[static_cast<size_t>(m) * B * 512 + j * 32];
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const uint4& q4 = wq[r][j >> 2];
-            const uint32_t w = (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
-            word_dot(w, zbe[r], zbo[r], xv, c[r][m]);
-          }
+        for (int sg = 0; sg < NSEG; ++sg) {
+          const int g = g0 + sg;
+          s[r][sg] = __half2float(scales[static_cast<size_t>(row) * G + g]);
+          const uint32_t z =
+              (__ldg(zeros + static_cast<size_t>(row) * ZW + g / PW) >> ((g % PW) * BITS)) & QMASK;
+          zbe[r][sg] = (0x6400u | z) * 0x00010001u;          // (1024 + z, 1024 + z)
+          zbo[r][sg] = (0x5400u | (z << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
         }
       }
+      float c4[R][MM][4];
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int m = 0; m < MM; ++m)
-          acc[r][m] = fmaf(s[r], (c[r][m][0] + c[r][m][1]) + (c[r][m][2] + c[r][m][3]), acc[r][m]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) c4[r][m][i] = 0.f;
+      // a finished segment: its step times its sum joins the row sum
+      auto fold = [&](int sg) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int m = 0; m < MM; ++m) {
+            acc[r][m] = fmaf(s[r][sg], (c4[r][m][0] + c4[r][m][1]) + (c4[r][m][2] + c4[r][m][3]),
+                             acc[r][m]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c4[r][m][i] = 0.f;
+          }
+      };
+      const uint4* xp = xs + static_cast<size_t>(b) * XB + lane;
+      auto word = [&](int r, int j) {
+        const uint4& q4 = wq[r][j >> 2];
+        return (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
+      };
+      if constexpr (BITS == 4) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+#pragma unroll
+          for (int m = 0; m < MM; ++m) {
+            const uint4 xv = xp[static_cast<size_t>(m) * B * XB + j * 32];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+              word_dot(word(r, j), zbe[r][j / SEGW], zbo[r][j / SEGW], xv, c4[r][m]);
+          }
+          if (j % SEGW == SEGW - 1) fold(j / SEGW);
+        }
+      } else {
+#pragma unroll
+        for (int o = 0; o < 8; ++o) {
+#pragma unroll
+          for (int m = 0; m < MM; ++m) {
+            const uint4 xv = xp[static_cast<size_t>(m) * B * XB + o * 32];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              word_dot8(word(r, 2 * o), zbe[r][(2 * o) / SEGW], xv.x, xv.y, c4[r][m]);
+              word_dot8(word(r, 2 * o + 1), zbe[r][(2 * o) / SEGW], xv.z, xv.w, c4[r][m]);
+            }
+          }
+          if ((2 * o + 1) % SEGW == SEGW - 1) fold((2 * o) / SEGW);
+        }
+      }
     }
   }
   if (cur >= 0) flush(cur);
@@ -380,31 +440,36 @@ int num_sms() {
   return cached;
 }
 
-template <int MM, int R, int kWarps, int MINB, bool SILU>
+template <int MM, int R, int kWarps, int MINB, bool SILU, int BITS, int GS>
 int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
                  const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
                  cudaStream_t st) {
+  constexpr int CK = BITS == 4 ? 128 : 64;
+  constexpr int XB = 32 * (CK / 8);
   // activation bytes a CTA may hold: a quarter of an SM's shared memory for
   // the half-SM shape, most of it otherwise
   constexpr int64_t kXsBudget = MINB == 2 ? 64 * 1024 : 160 * 1024;
-  const int G = K / kGroup;
-  // K slices: activations of a slice take MM * 8 KB per 32 groups; split K
-  // only when the whole row does not fit the budget
+  const int K128 = K / 128;
+  // K slices, in whole 128-channel units: the activations of a slice take
+  // MM * XB * 16 bytes per block of 32 lane chunks; split K only when the
+  // whole row does not fit the budget
+  auto xs_bytes = [&](int ns) {
+    const int chunks = ((K128 + ns - 1) / ns) * (128 / CK);
+    return static_cast<int64_t>(MM) * ((chunks + 31) / 32) * XB * 16;
+  };
   int nsplit = 1;
-  while (nsplit < kMaxSplit &&
-         static_cast<int64_t>(MM) * (((G + nsplit - 1) / nsplit + 31) / 32) * 8192 > kXsBudget)
-    ++nsplit;
-  const int gs = (G + nsplit - 1) / nsplit;
-  const int KS = gs * kGroup;
+  while (nsplit < kMaxSplit && xs_bytes(nsplit) > kXsBudget) ++nsplit;
+  const int ks = (K128 + nsplit - 1) / nsplit;
+  const int KS = ks * 128;
   nsplit = (K + KS - 1) / KS;
-  const int B = (gs + 31) / 32;
+  const int B = (ks * (128 / CK) + 31) / 32;
   // balancing units: row units, or (gate, up) pairs
   const int units = SILU ? N / 2 : N / R;
   int gx = num_sms() / nsplit;
   if (gx > units) gx = units;
   if (gx < 1) gx = 1;
   const int rows_cap = ((units + gx - 1) / gx) * (SILU ? 2 : R);
-  const size_t smem = static_cast<size_t>(MM) * B * 512 * sizeof(uint4) +
+  const size_t smem = static_cast<size_t>(MM) * B * XB * sizeof(uint4) +
                       (MM <= 2 ? static_cast<size_t>(MM) * kWarps * rows_cap * sizeof(float)
                                : static_cast<size_t>(MM) * rows_cap * sizeof(float) +
                                      static_cast<size_t>(kWarps) * 2 * R * MM * sizeof(float));
@@ -413,10 +478,11 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
               "use awq_gemm)", smem, N, K, MM);
     return AWQ_ERR_SHAPE;
   }
+  auto kern = gemv_kernel<MM, R, kWarps, MINB, SILU, BITS, GS>;
   static bool attr_set = false;
   if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemv_kernel<MM, R, kWarps, MINB, SILU>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024));
+    AWQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      220 * 1024));
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -433,37 +499,42 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = nsplit > 1 ? 2 : 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_kernel<MM, R, kWarps, MINB, SILU>, X, qweight, scales,
-                                  zeros, inv_s, N, K, KS, rows_cap, Y));
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, X, qweight, scales, zeros, inv_s, N, K, KS,
+                                  rows_cap, Y));
   return AWQ_OK;
 }
 
-template <int MM, bool SILU>
+template <int MM, bool SILU, int BITS, int GS>
 int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
               const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
               cudaStream_t st) {
   if constexpr (MM <= 2) {
-    const size_t code_bytes = static_cast<size_t>(N) * K / 2;
-    if (code_bytes <= kSmallBytesPerSm * num_sms())
-      return launch_shape<MM, 2, 16, 2, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    return launch_shape<MM, 2, 32, 1, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    // the half-SM shape for the smallest layers of the default format only
+    constexpr bool kDefault = BITS == 4 && GS == 128;
+    const size_t code_bytes = static_cast<size_t>(N) * K * BITS / 8;
+    if (kDefault && code_bytes <= kSmallBytesPerSm * num_sms())
+      return launch_shape<MM, 2, 16, 2, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K,
+                                                        Y, st);
+    return launch_shape<MM, 2, 32, 1, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y,
+                                                      st);
   } else {
-    return launch_shape<MM, 1, 16, 1, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    return launch_shape<MM, 1, 16, 1, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y,
+                                                      st);
   }
 }
 
-template <bool SILU>
+template <bool SILU, int BITS, int GS>
 int launch_m(const __half* X, int M, const uint32_t* qweight, const __half* scales,
              const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y, cudaStream_t st) {
   switch (M) {
-    case 1: return launch_mm<1, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 2: return launch_mm<2, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 3: return launch_mm<3, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 4: return launch_mm<4, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 5: return launch_mm<5, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 6: return launch_mm<6, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 7: return launch_mm<7, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
-    case 8: return launch_mm<8, SILU>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 1: return launch_mm<1, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 2: return launch_mm<2, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 3: return launch_mm<3, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 4: return launch_mm<4, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 5: return launch_mm<5, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 6: return launch_mm<6, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 7: return launch_mm<7, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
+    case 8: return launch_mm<8, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y, st);
     default: set_error("awq_gemv: M = %d must be in [1, 8]", M); return AWQ_ERR_SHAPE;
   }
 }
@@ -472,9 +543,26 @@ int launch_m(const __half* X, int M, const uint32_t* qweight, const __half* scal
 
 int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* scales,
                 const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
-                cudaStream_t st, bool silu_mul) {
-  if (silu_mul) return launch_m<true>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
-  return launch_m<false>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
+                cudaStream_t st, bool silu_mul, int w_bit, int group) {
+  if (silu_mul) {
+    if (w_bit != 4 || group != 128) {
+      set_error("the fused gate/up layer takes 4-bit codes with 128-channel groups");
+      return AWQ_ERR_UNSUPPORTED;
+    }
+    return launch_m<true, 4, 128>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
+  }
+#define AWQ_GEMV_CASE(B, GS)                                                              \
+  if (w_bit == B && group == GS)                                                          \
+    return launch_m<false, B, GS>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
+  AWQ_GEMV_CASE(4, 128)
+  AWQ_GEMV_CASE(4, 64)
+  AWQ_GEMV_CASE(4, 32)
+  AWQ_GEMV_CASE(8, 128)
+  AWQ_GEMV_CASE(8, 64)
+  AWQ_GEMV_CASE(8, 32)
+#undef AWQ_GEMV_CASE
+  set_error("awq_gemv: w_bit = %d, group = %d is not supported", w_bit, group);
+  return AWQ_ERR_UNSUPPORTED;
 }
 
 }  // namespace awq

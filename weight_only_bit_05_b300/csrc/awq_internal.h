@@ -13,15 +13,19 @@ int launch_channel_scales(const float* a, int K, double alpha, float* s_c, float
                           cudaStream_t st);
 
 // awq_pack.cu
+// w_bit 4 or 8, group 128/64/32, zero_point on (asymmetric) or off
+// (symmetric: codes offset by 2^(w_bit-1), stored as the zero point).
 int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweight,
-                __half* scales, uint32_t* zeros, cudaStream_t st);
+                __half* scales, uint32_t* zeros, cudaStream_t st, int w_bit = 4,
+                int group = 128, bool zero_point = true);
 
 // awq_gemv.cu
 // silu_mul: the weight's N rows are I = N/2 gate rows over I up rows and Y
 // receives silu(gate) * up, [M][N/2].
+// w_bit 4 or 8 and group 128/64/32 give the packed layout (silu_mul: 4/128).
 int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* scales,
                 const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
-                cudaStream_t st, bool silu_mul = false);
+                cudaStream_t st, bool silu_mul = false, int w_bit = 4, int group = 128);
 
 // awq_fold.cu
 int launch_fold_inv_scales(const __half* W, int64_t rows, int64_t cols, const float* inv_s,
@@ -29,10 +33,12 @@ int launch_fold_inv_scales(const __half* W, int64_t rows, int64_t cols, const fl
 
 // awq_gemm.cu
 enum GemmMode { kGemmOutF16 = 0, kGemmSqErr = 1, kGemmDenseF32 = 2, kGemmSiluF16 = 3 };
-// Xt = fp16(X * inv_s), each 8-element chunk of k stored as (k0,k4) (k1,k5)
-// (k2,k6) (k3,k7): the layout launch_gemm takes with xt_permuted = true.
+// Xt = fp16(X * inv_s), each 8-element chunk of k stored in the pair order of
+// the dequantization of w_bit-bit codes ((k0,k4) (k1,k5) (k2,k6) (k3,k7) for 4,
+// (k0,k2) (k1,k3) (k4,k6) (k5,k7) for 8): the layout launch_gemm takes with
+// xt_permuted = true.
 int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __half* Xt,
-                    cudaStream_t st);
+                    cudaStream_t st, int w_bit = 4);
 // Runs the tensor-core kernel on activations `Xt` [M][K] (already scaled;
 // xt_permuted says whether k is in the prescale kernel's chunk order, which
 // the quantized modes prefer, or natural).
@@ -44,7 +50,8 @@ int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __hal
 //                  out = fp16 silu(gate) * up, [M][ldo] with N/2 columns
 int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
                 const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
-                void* out, int ldo, const float* yref, int ldy, cudaStream_t st);
+                void* out, int ldo, const float* yref, int ldy, cudaStream_t st, int w_bit = 4,
+                int group = 128);
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
 

@@ -1,33 +1,42 @@
-// Scaled group round-to-nearest with zero point, and packing.
+// Scaled group round-to-nearest, and packing.
 //
 // "AWQ量化实战：无需重训，把大模型压进4bit显存" §1.1 (round to nearest), §2.1 (the
-// channel is the input dimension of the out x in weight), §2.3 (128
-// consecutive input channels share one step); "大模型量化部署实战：GPTQ与AWQ算法",
-// section 大模型量化的核心原理与位宽选择 (a scale plus a zero point per group).
+// channel is the input dimension of the out x in weight), §2.3 (GS = 128,
+// also 64 or 32, consecutive input channels share one step), §3.3 (zero
+// point off is the symmetric form; 8 bits is the conservative width);
+// "大模型量化部署实战：GPTQ与AWQ算法", section 大模型量化的核心原理与位宽选择 (a scale
+// plus a zero point per group; int4 spans -8..7).
 //
-// One warp owns row n and 8 consecutive groups (1024 input channels, the span
-// of one zero-point word).  Lane l holds 32 consecutive weights (a quarter
-// group): four lanes reduce a group's min/max with two shuffles, every lane
-// decides its 32 codes in fp32 with IEEE division and round-half-even (the
-// same operations, in the same precision, as the definition), writes one
-// 16-byte word quad, and the warp ORs the 8 zero points into one word.
+// One warp owns row n and 1024 consecutive input channels.  Lane l holds 32
+// consecutive weights: GS/32 lanes reduce a group's min/max with shuffles,
+// every lane decides its 32 codes in fp32 with IEEE division and
+// round-half-even (the same operations, in the same precision, as the
+// definition), writes its 32 codes as one or two 16-byte stores, and the
+// warp ORs the groups' zero points into their words.
 #include "awq_internal.h"
 
 namespace awq {
 namespace {
 
+template <int BITS, int GS, bool ZP>
 __global__ void __launch_bounds__(256)
     quant_pack_kernel(const __half* __restrict__ W, const float* __restrict__ s_c, int N, int K,
                       uint32_t* __restrict__ qweight, __half* __restrict__ scales,
                       uint32_t* __restrict__ zeros) {
-  const int G = K / kGroup;
-  const int units = (G + 7) / 8;                  // zero-point words per row
+  constexpr int kPerWord = 32 / BITS;             // codes per packed word
+  constexpr int kQmax = (1 << BITS) - 1;
+  constexpr int kHalf = 1 << (BITS - 1);
+  constexpr int kLanesPerGroup = GS / 32;
+  constexpr int kZWords = (1024 / GS) / kPerWord;   // zero-point words per warp span
+  const int G = K / GS;
+  const int ZW = (G + kPerWord - 1) / kPerWord;   // zero-point words per row
+  const int units = (K + 1023) / 1024;            // warp spans per row
   const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (gw >= N * units) return;
   const int lane = threadIdx.x & 31;
   const int n = gw / units, u = gw - n * units;
   const int k0 = u * 1024 + lane * 32;            // this lane's first input channel
-  const bool valid = k0 < K;                      // whole quarter groups only (K % 128 == 0)
+  const bool valid = k0 < K;                      // whole lanes only (K % 128 == 0)
 
   float w[32];
   if (valid) {
@@ -65,53 +74,90 @@ __global__ void __launch_bounds__(256)
     mn = fminf(mn, w[i]);
     mx = fmaxf(mx, w[i]);
   }
-  // min/max over the 4 lanes of the group (lanes 4g..4g+3)
+  // min/max over the lanes of the group
 #pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
+  for (int off = 1; off < kLanesPerGroup; off <<= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
 
-  float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+  float s32 = ZP ? __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kQmax))
+                 : __fdiv_rn(fmaxf(fabsf(mn), fabsf(mx)), static_cast<float>(kHalf - 1));
   s32 = fminf(fmaxf(s32, 6.103515625e-05f), 65504.0f);   // [2^-14, 65504]
   const __half s16 = __float2half_rn(s32);
   const float s = __half2float(s16);
-  const float z = fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.f), 15.f);
+  const float z = ZP ? fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.f), static_cast<float>(kQmax))
+                     : static_cast<float>(kHalf);
 
-  uint32_t words[4];
+  constexpr int kWords = 32 / kPerWord;           // packed words of this lane
+  uint32_t words[kWords];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
+  for (int v = 0; v < kWords; ++v) {
     uint32_t word = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float q = fminf(fmaxf(rintf(__fdiv_rn(w[v * 8 + i], s)) + z, 0.f), 15.f);
-      word |= static_cast<uint32_t>(q) << (4 * i);
+    for (int i = 0; i < kPerWord; ++i) {
+      const float r = rintf(__fdiv_rn(w[v * kPerWord + i], s));
+      const float q = ZP ? fminf(fmaxf(r + z, 0.f), static_cast<float>(kQmax))
+                         : fminf(fmaxf(r, static_cast<float>(-kHalf)),
+                                 static_cast<float>(kHalf - 1)) + static_cast<float>(kHalf);
+      word |= static_cast<uint32_t>(q) << (BITS * i);
     }
     words[v] = word;
   }
 
-  const int g = k0 / kGroup;
+  const int g = k0 / GS;
+  const bool leader = valid && (lane % kLanesPerGroup) == 0;
   if (valid) {
-    uint4* dst = reinterpret_cast<uint4*>(qweight + static_cast<size_t>(n) * (K / 8) + k0 / 8);
-    *dst = make_uint4(words[0], words[1], words[2], words[3]);
-    if ((lane & 3) == 0) scales[static_cast<size_t>(n) * G + g] = s16;
+    uint4* dst = reinterpret_cast<uint4*>(qweight + static_cast<size_t>(n) * (K / kPerWord) +
+                                          k0 / kPerWord);
+#pragma unroll
+    for (int v = 0; v < kWords / 4; ++v)
+      dst[v] = make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]);
+    if (leader) scales[static_cast<size_t>(n) * G + g] = s16;
   }
-  const uint32_t zc = (valid && (lane & 3) == 0) ? static_cast<uint32_t>(z) << (4 * (g & 7)) : 0u;
-  const uint32_t zword = __reduce_or_sync(0xffffffffu, zc);
-  if (lane == 0) zeros[static_cast<size_t>(n) * units + u] = zword;
+  // the zero points of this warp's groups, kPerWord to a word
+  const int gl = g - u * (1024 / GS);             // group index within the warp span
+#pragma unroll
+  for (int zw = 0; zw < kZWords; ++zw) {
+    const uint32_t zc = (leader && gl / kPerWord == zw)
+                            ? static_cast<uint32_t>(z) << (BITS * (gl % kPerWord)) : 0u;
+    const uint32_t zword = __reduce_or_sync(0xffffffffu, zc);
+    const int col = u * kZWords + zw;
+    if (lane == 0 && col < ZW) zeros[static_cast<size_t>(n) * ZW + col] = zword;
+  }
 }
 
 }  // namespace
 
 int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweight,
-                __half* scales, uint32_t* zeros, cudaStream_t st) {
-  const int units = (K / kGroup + 7) / 8;
+                __half* scales, uint32_t* zeros, cudaStream_t st, int w_bit, int group,
+                bool zero_point) {
+  const int units = (K + 1023) / 1024;
   const int64_t warps = static_cast<int64_t>(N) * units;
-  const int64_t blocks = (warps + 7) / 8;
-  quant_pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(W, s_c, N, K, qweight, scales,
-                                                                   zeros);
-  AWQ_CUDA_TRY_LAUNCH("quant_pack_kernel");
-  return AWQ_OK;
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+#define AWQ_PACK_CASE(B, GS, ZP)                                                         \
+  if (w_bit == B && group == GS && zero_point == ZP) {                                   \
+    quant_pack_kernel<B, GS, ZP><<<blocks, 256, 0, st>>>(W, s_c, N, K, qweight, scales, \
+                                                         zeros);                        \
+    AWQ_CUDA_TRY_LAUNCH("quant_pack_kernel");                                            \
+    return AWQ_OK;                                                                       \
+  }
+  AWQ_PACK_CASE(4, 128, true)
+  AWQ_PACK_CASE(4, 64, true)
+  AWQ_PACK_CASE(4, 32, true)
+  AWQ_PACK_CASE(4, 128, false)
+  AWQ_PACK_CASE(4, 64, false)
+  AWQ_PACK_CASE(4, 32, false)
+  AWQ_PACK_CASE(8, 128, true)
+  AWQ_PACK_CASE(8, 64, true)
+  AWQ_PACK_CASE(8, 32, true)
+  AWQ_PACK_CASE(8, 128, false)
+  AWQ_PACK_CASE(8, 64, false)
+  AWQ_PACK_CASE(8, 32, false)
+#undef AWQ_PACK_CASE
+  set_error("awq_pack: w_bit = %d, group = %d, zero_point = %d is not supported", w_bit, group,
+            static_cast<int>(zero_point));
+  return AWQ_ERR_UNSUPPORTED;
 }
 
 }  // namespace awq

@@ -44,14 +44,16 @@ SearchLayout layout(int64_t T, int N, int K, int n_grid) {
   const int64_t n_up = (N + 127) / 128 * 128;
   if (rows > n_up) rows = n_up;
   L.chunk_rows = static_cast<int>(rows);
-  const int G = K / kGroup, ZW = (G + 7) / 8;
+  // packed buffers sized for the largest variant (8-bit codes, 32-channel
+  // groups), so that one workspace size serves every configuration
+  const int G = K / 32, ZW = (G + 3) / 4;
   size_t o = 0;
   L.off_a = o; o += align256(static_cast<size_t>(K) * 4);
   L.off_sc = o; o += align256(static_cast<size_t>(n_grid) * K * 4);
   L.off_inv = o; o += align256(static_cast<size_t>(n_grid) * K * 4);
   L.off_stats = o; o += align256(absmean_workspace_size(T, K));
   L.off_xt = o; o += align256(static_cast<size_t>(T) * K * 2);
-  L.off_qw = o; o += align256(static_cast<size_t>(rows) * K / 2);
+  L.off_qw = o; o += align256(static_cast<size_t>(rows) * K);
   L.off_sc16 = o; o += align256(static_cast<size_t>(rows) * G * 2);
   L.off_zr = o; o += align256(static_cast<size_t>(rows) * ZW * 4);
   L.off_yref = o; o += align256(static_cast<size_t>(T) * rows * 4);
@@ -106,7 +108,8 @@ int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32
                       float* inv_s_out, int32_t* best_out, double* mse_out, double* row_err_out,
                       void* stream) {
   const awq_config c = cfg ? *cfg : awq_default_config();
-  if (c.w_bit != 4 || c.group != 128 || c.zero_point != 1 || c.n_grid < 1 || c.n_grid > 64) {
+  if ((c.w_bit != 4 && c.w_bit != 8) || (c.group != 128 && c.group != 64 && c.group != 32) ||
+      (c.zero_point != 0 && c.zero_point != 1) || c.n_grid < 1 || c.n_grid > 64) {
     set_error("awq_search_scales: unsupported configuration w_bit=%d group=%d zero_point=%d "
               "n_grid=%d", c.w_bit, c.group, c.zero_point, c.n_grid);
     return AWQ_ERR_UNSUPPORTED;
@@ -175,10 +178,11 @@ int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32
     TRY(launch_gemm(kGemmDenseF32, X, false, static_cast<int>(T), nullptr, nullptr, nullptr, Wc,
                     rows, K, yref, rows, nullptr, 0, st));
     for (int i = 0; i < n_grid; ++i) {
-      TRY(launch_pack(Wc, sc_all + static_cast<size_t>(i) * K, rows, K, qw, sc16, zr, st));
-      TRY(launch_prescale(X, inv_all + static_cast<size_t>(i) * K, T, K, xt, st));
+      TRY(launch_pack(Wc, sc_all + static_cast<size_t>(i) * K, rows, K, qw, sc16, zr, st,
+                      c.w_bit, c.group, c.zero_point != 0));
+      TRY(launch_prescale(X, inv_all + static_cast<size_t>(i) * K, T, K, xt, st, c.w_bit));
       TRY(launch_gemm(kGemmSqErr, xt, true, static_cast<int>(T), qw, sc16, zr, nullptr, rows, K,
-                      part, rows, yref, rows, st));
+                      part, rows, yref, rows, st, c.w_bit, c.group));
       rows_reduce_kernel<<<(rows + 255) / 256, 256, 0, st>>>(
           part, slots, rows, rows, row_err + static_cast<size_t>(i) * N + r0);
       AWQ_CUDA_TRY_LAUNCH("rows_reduce_kernel");
