@@ -346,6 +346,164 @@ def gemv_70b(awq, torch, hbm, reps=20):
     return out
 
 
+def fused_gate_up(awq, torch, hbm, pk, reps=20):
+    """The fused gate/up projection (silu(gate) * up from one stacked weight)
+    next to the plain layer of the same weight, on the 7B gate/up shape: the
+    GEMV at M = 1 (GB/s, rotating weight copies) and the tensor-core GEMM at
+    M = 2048 (TFLOP/s)."""
+    dev = torch.device("cuda")
+    K, N, lid = awq_inputs.layer(MODEL, "gate_up")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + lid)
+    qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
+    inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+    nbytes = gemv_bytes(1, N, K)
+    ncp = max(4, -(-3 * 126 * 2**20 // nbytes))
+    copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(ncp - 1)]
+    X1 = torch.randn((1, K), generator=gen, device=dev).half()
+    Y1 = torch.empty((1, N), dtype=torch.float16, device=dev)
+
+    def timed(fn, n_per):
+        g = capture(torch, fn)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000 / (reps * n_per)
+
+    out = {"shape": f"{MODEL} gate_up {K}->{N} (I = {N // 2})"}
+    for label, fn in (("plain", awq.gemv), ("fused", awq.gemv_silu_mul)):
+        y = Y1 if label == "plain" else Y1[:, :N // 2]
+        us = timed(lambda fn=fn, y=y: [fn(X1, q, s_, z, inv_s, out=y) for q, s_, z in copies], ncp)
+        gbs = (nbytes - (N // 2 * 2 if label == "fused" else 0)) / us / 1e3
+        out[f"gemv_M1_{label}"] = {"us": round(us, 2), "GB/s": round(gbs, 1),
+                                   "frac": round(gbs / hbm, 4)}
+    del copies
+    M = 2048
+    X = torch.randn((M, K), generator=gen, device=dev).half()
+    Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    for label, fn in (("plain", awq.gemm), ("fused", awq.gemm_silu_mul)):
+        y = Y if label == "plain" else Y[:, :N // 2].contiguous()
+        us = timed(lambda fn=fn, y=y: fn(X, qw, sc, zs, inv_s, out=y, workspace=ws), 1)
+        tf = 2.0 * M * N * K / us / 1e6
+        out[f"gemm_M{M}_{label}"] = {"us": round(us, 1), "TFLOP/s": round(tf, 1),
+                                     "frac": round(tf / peak, 4)}
+    del X, Y, ws, qw, sc, zs
+    torch.cuda.empty_cache()
+    return out
+
+
+VARIANTS = [(4, 128, True), (4, 128, False), (4, 64, True), (4, 32, True), (8, 128, True),
+            (8, 32, False)]
+
+
+def variants(awq, torch, hbm, pk, reps=20):
+    """The quantization variants (bit width, group size, zero point) on the 7B
+    gate/up shape: GEMV at M = 1 (GB/s over rotating weight copies) and the
+    tensor-core GEMM at M = 2048 (TFLOP/s)."""
+    dev = torch.device("cuda")
+    K, N, lid = awq_inputs.layer(MODEL, "gate_up")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + lid)
+    W = (torch.randn((N, K), generator=gen, device=dev) * 0.02).half()
+    inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+    X1 = torch.randn((1, K), generator=gen, device=dev).half()
+    Y1 = torch.empty((1, N), dtype=torch.float16, device=dev)
+    M = 2048
+    X = torch.randn((M, K), generator=gen, device=dev).half()
+    Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    out = {"shape": f"{MODEL} gate_up {K}->{N}"}
+
+    def timed(fn, n_per):
+        g = capture(torch, fn)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000 / (reps * n_per)
+
+    for w_bit, group, zp in VARIANTS:
+        qw, sc, zs = awq.pack(W, None, w_bit=w_bit, group=group, zero_point=zp)
+        G = K // group
+        c = 32 // w_bit
+        nbytes = N * K * w_bit // 8 + 2 * N * G + 4 * N * (-(-G // c)) + 2 * K + 4 * K + 2 * N
+        ncp = max(4, -(-3 * 126 * 2**20 // nbytes))
+        copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(ncp - 1)]
+        us1 = timed(lambda: [awq.gemv(X1, q, s_, z, inv_s, out=Y1) for q, s_, z in copies], ncp)
+        del copies
+        us2 = timed(lambda: awq.gemm(X, qw, sc, zs, inv_s, out=Y, workspace=ws), 1)
+        tf = 2.0 * M * N * K / us2 / 1e6
+        out[f"w{w_bit} g{group} {'asym' if zp else 'sym'}"] = {
+            "gemv_M1_us": round(us1, 2), "gemv_M1_GB/s": round(nbytes / us1 / 1e3, 1),
+            "gemv_M1_frac": round(nbytes / us1 / 1e3 / hbm, 4),
+            "gemm_M2048_TFLOP/s": round(tf, 1), "gemm_frac": round(tf / peak, 4)}
+        del qw, sc, zs
+    del W, X, Y, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+SWEEP_M = (1, 4, 8, 16, 64, 128, 256, 512, 1024, 2048, 4096)
+
+
+def sweep_70b(awq, torch, hbm, pk, reps=5):
+    """The Llama-2-70B layers over the token count M: awq_gemv for M <= 8,
+    awq_gemm above; GB/s of the algorithmic bytes and TFLOP/s of 2 M N K."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    out = {}
+    for name in ("qkv", "o", "gate_up", "down"):
+        K, N, lid = awq_inputs.layer("llama2-70b", name)
+        gen.manual_seed(1000 + lid)
+        qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
+        inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+        row = {}
+        for M in SWEEP_M:
+            X = torch.randn((M, K), generator=gen, device=dev).half()
+            Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            if M <= 8:
+                fn = lambda X=X, Y=Y: awq.gemv(X, qw, sc, zs, inv_s, out=Y)
+            else:
+                ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+                fn = lambda X=X, Y=Y, ws=ws: awq.gemm(X, qw, sc, zs, inv_s, out=Y, workspace=ws)
+            g = capture(torch, fn)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1000 / reps
+            gbs = gemv_bytes(M, N, K) / us / 1e3
+            tf = 2.0 * M * N * K / us / 1e6
+            row[f"M{M}"] = {"us": round(us, 1), "GB/s": round(gbs, 1), "TFLOP/s": round(tf, 1),
+                            "hbm_frac": round(gbs / hbm, 3), "tensor_frac": round(tf / peak, 3)}
+            del g, X, Y
+        out[f"{name} {K}->{N}"] = row
+        del qw, sc, zs
+        torch.cuda.empty_cache()
+    return {"note": "weights of one layer, L2-resident for the small ones: an upper bound on "
+                    "decode GB/s, exact for the tensor-bound M", "layers": out}
+
+
 def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
     """Wall time of awq_search_scales on one layer (20 alphas) and the
     TFLOP/s of its tensor-core work (Y_ref once + 20 squared-error passes)."""
@@ -385,6 +543,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-search", action="store_true", help="skip the scale-search timing")
     ap.add_argument("--no-70b", action="store_true", help="skip the 70B-shape GEMV figures")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused gate/up figures")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 70B token-count sweep")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the quantization-variant figures")
     ap.add_argument("--only-gemm", default=None, metavar="MODEL:LAYER:M",
                     help="run only awq_gemm on one shape 3 times (a small case for profilers)")
     args = ap.parse_args()
@@ -524,6 +686,9 @@ def main():
 
     gemm = None if args.no_gemm else gemm_prefill(awq, torch, pk)
     g70 = None if args.no_70b else gemv_70b(awq, torch, hbm)
+    fused = None if args.no_fused else fused_gate_up(awq, torch, hbm, pk)
+    var = None if args.no_variants else variants(awq, torch, hbm, pk)
+    sweep = None if args.no_sweep else sweep_70b(awq, torch, hbm, pk)
     search = None if args.no_search else search_run(awq, torch)
     awq.check_device_error()
 
@@ -559,6 +724,9 @@ def main():
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gemv_70b": g70,
+        "fused_gate_up": fused,
+        "variants": var,
+        "sweep_70b": sweep,
         "gemm_prefill": gemm,
         "search": search,
     }

@@ -167,7 +167,11 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
  * memory). ("awq-quantization" skill page, 主要功能: the GEMM kernel serves
  * batch > 1.) When inv_s is not NULL, X~ = fp16(X * inv_s) is first written
  * to the workspace; with inv_s == NULL X is read directly and the workspace
- * may be NULL. Y: fp16 [M][N]. */
+ * may be NULL. awq_gemm_workspace_size also counts the fp32 partial sums of a
+ * split-K launch (chosen when the layer has too few 128-row tiles to fill the
+ * GPU; the splits are added in a fixed order by a second kernel): a smaller
+ * workspace, at least X~ when inv_s is given, runs without split-K.
+ * Y: fp16 [M][N]. */
 AWQ_API size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K);
 AWQ_API int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight,
              const uint16_t* scales, const uint32_t* zeros, const float* inv_s,

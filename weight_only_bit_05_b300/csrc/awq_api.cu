@@ -264,10 +264,15 @@ int awq_fold_inv_scales(const uint16_t* W, int64_t rows, int64_t cols, const flo
                                 reinterpret_cast<__half*>(out), static_cast<cudaStream_t>(stream));
 }
 
-size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {
-  (void)N;
-  if (M <= 0 || K <= 0) return 0;
+namespace {
+size_t xt_bytes(int32_t M, int32_t K) {
   return ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256;
+}
+}  // namespace
+
+size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {
+  if (M <= 0 || K <= 0 || N <= 0 || K % kGroup != 0) return 0;
+  return xt_bytes(M, K) + gemm_partial_bytes(M, N, K);
 }
 
 namespace {
@@ -291,19 +296,26 @@ int gemm_common(int mode, const awq_config* cfg, const uint16_t* X, int32_t M,
   AWQ_TRY(check_ptr(Y, "Y"));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const __half* xt = reinterpret_cast<const __half*>(X);
+  // workspace: X~ first (when inv_s is given), then the split-K partial sums
+  // if the rest of the workspace holds them
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  size_t rest = ws_bytes;
   if (inv_s) {
-    if (!workspace || !aligned16(workspace) || ws_bytes < awq_gemm_workspace_size(M, N, K)) {
+    if (!workspace || !aligned16(workspace) || ws_bytes < xt_bytes(M, K)) {
       set_error("awq_gemm: workspace must be 16-B aligned and >= %zu bytes",
                 awq_gemm_workspace_size(M, N, K));
       return AWQ_ERR_WORKSPACE;
     }
-    __half* w = static_cast<__half*>(workspace);
+    __half* w = reinterpret_cast<__half*>(ws);
     AWQ_TRY(launch_prescale(xt, inv_s, M, K, w, st, c.w_bit));
     xt = w;
+    ws += xt_bytes(M, K);
+    rest -= xt_bytes(M, K);
   }
+  float* part = (ws && aligned16(ws)) ? reinterpret_cast<float*>(ws) : nullptr;
   return launch_gemm(mode, xt, inv_s != nullptr, M, qweight,
                      reinterpret_cast<const __half*>(scales), zeros, nullptr, N, K, Y, ldy,
-                     nullptr, 0, st, c.w_bit, c.group);
+                     nullptr, 0, st, c.w_bit, c.group, part, part ? rest : 0);
 }
 
 }  // namespace

@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_a,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros, int M,
                 int N, int K, int gs, void* __restrict__ out, int ldo,
-                const float* __restrict__ yref, int ldy) {
+                const float* __restrict__ yref, int ldy, int splits, int kps,
+                float* __restrict__ part) {
   using C = Cfg<BN, MODE, BITS>;
   constexpr int KWB = BK * BITS / 32;   // packed words of one row per stage
   constexpr int S = C::STAGES;
@@ -189,6 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = K / BK;
   const int n_tiles = (N + BM - 1) / BM;
   const int tiles = n_tiles * ((M + BN - 1) / BN);
+  // split-K: work item t is tile t / splits over the k-blocks [kb0, kb1) of
+  // split t % splits, kps of them (an even number, so that no split starts
+  // inside a 128-channel group; the host guarantees every split is
+  // non-empty); with splits > 1 the epilogue writes fp32 partial sums to
+  // part[split][M][ldo] and a second kernel adds them
+  const int items = tiles * splits;
+  auto krange = [&](int t, int& kb0, int& kb1) {
+    kb0 = (t % splits) * kps;
+    kb1 = kb0 + kps < nk ? kb0 + kps : nk;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -224,9 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;   // k-blocks issued by this CTA over all its tiles
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int n0 = (t % n_tiles) * BM, m0 = (t / n_tiles) * BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+      for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
+        const int tile = t / splits;
+        const int n0 = (tile % n_tiles) * BM, m0 = (tile / n_tiles) * BN;
+        int kb0, kb1;
+        krange(t, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
           if (it >= S && !wait_or_abort(empty + s, ((it / S) - 1) & 1, ab, 1u)) {
             ok = false;
@@ -265,12 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
       int it = 0, lt = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++lt) {
+      for (int t = blockIdx.x; t < items && ok; t += gridDim.x, ++lt) {
         const int b = lt & 1;
         if (lt >= 2 && !wait_or_abort(acc_empty + b, ((lt >> 1) - 1) & 1, ab, 2u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * C::ACC_COLS;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        int kb0, kb1;
+        krange(t, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!wait_or_abort(full + s, ph, ab, 2u) ||
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * C::B_BYTES));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           umma_commit(empty + s);
         }
         if (ok) umma_commit(acc_full + b);
@@ -306,17 +322,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int PW = 32 / BITS;        // codes per packed word
       constexpr uint32_t QMASK = (1u << BITS) - 1u;
       const int G = K / gs, ZW = (G + PW - 1) / PW;
-      // the groups this thread meets, in order: a new one every kb_per_g
-      // stages, gstride groups after the previous one
-      const int kb_per_g = gs >= BK ? gs / BK : 1;
+      // the groups this thread meets, in order: a new one every 2^kb_shift
+      // stages (2 for 128-channel groups, else 1), gstride groups after the
+      // previous one (2 for 32-channel groups, else 1); shifts, not divisions,
+      // on this per-stage path
+      const int kb_shift = gs > BK ? 1 : 0;
+      const int kb_mask = (1 << kb_shift) - 1;
       const int gstride = gs >= BK ? 1 : BK / gs;
       const int gfirst = (half * 32) / gs;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
         // with the fused gate/up weight, MMA row r of the tile is virtual row
         // v = n0 + r: gate row v/2 for even v, up row v/2 for odd v
-        const int v = (t % n_tiles) * BM + r;
+        const int v = ((t / splits) % n_tiles) * BM + r;
+        int kb0, kb1;
+        krange(t, kb0, kb1);
         const int n = MODE == kGemmSiluF16 ? (v >> 1) + (v & 1) * (N / 2) : v;
         const bool row_ok = MODE == kGemmSiluF16 ? (v >> 1) < N / 2 : v < N;
         const int raw_r = MODE == kGemmSiluF16 ? (r >> 1) + (r & 1) * (BM / 2) : r;
@@ -334,13 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
 #pragma unroll
-        for (int i = 0; i < kSzAhead; ++i) load_sz(i, sq[i], zq[i]);
+        for (int i = 0; i < kSzAhead; ++i) load_sz((kb0 >> kb_shift) + i, sq[i], zq[i]);
         uint32_t zbe = 0x64006400u, zbo = 0x54005400u;
         __half2 s2 = __half2half2(__ushort_as_half(0));
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
-          if (kb % kb_per_g == 0) {
-            const int gi = kb / kb_per_g;   // this thread's group counter
+          if ((kb & kb_mask) == 0) {
+            const int gi = kb >> kb_shift;   // this thread's group counter
             s2 = __half2half2(sq[0]);
             zbe = (0x6400u | zq[0]) * 0x00010001u;          // (1024 + z, 1024 + z)
             zbo = (0x5400u | (zq[0] << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
@@ -386,8 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     int lt = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
-      const int n0 = (t % n_tiles) * BM, mt = t / n_tiles, m0 = mt * BN;
+    for (int t = blockIdx.x; t < items; t += gridDim.x, ++lt) {
+      const int tile = t / splits;
+      const int n0 = (tile % n_tiles) * BM, mt = tile / n_tiles, m0 = mt * BN;
+      float* pout = part + static_cast<size_t>(t % splits) * M * ldo;   // splits > 1
       const int b = lt & 1;
       const int n = n0 + quarter * 32 + lane;
       if (!wait_or_abort(acc_full + b, (lt >> 1) & 1, ab, 8u)) break;
@@ -421,7 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float val = __uint_as_float(v[j]);
               const size_t idx = static_cast<size_t>(m) * ldo + n;
               if (MODE == kGemmOutF16) {
-                static_cast<__half*>(out)[idx] = __float2half_rn(val);
+                if (splits > 1)
+                  pout[idx] = val;
+                else
+                  static_cast<__half*>(out)[idx] = __float2half_rn(val);
               } else if (MODE == kGemmDenseF32) {
                 static_cast<float*>(out)[idx] = val;
               } else {
@@ -476,11 +502,33 @@ __global__ void prescale_kernel(const __half* __restrict__ X, const float* __res
   reinterpret_cast<uint4*>(Xt)[i] = o;
 }
 
+// Y[m][n] = fp16(sum over s of part[s][m][n]), the splits added in order.
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t mn4,
+                                     __half* __restrict__ Y) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < mn4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = reinterpret_cast<const float4*>(part)[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = reinterpret_cast<const float4*>(part)[s * mn4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    reinterpret_cast<__half2*>(Y)[2 * i] = __floats2half2_rn(a.x, a.y);
+    reinterpret_cast<__half2*>(Y)[2 * i + 1] = __floats2half2_rn(a.z, a.w);
+  }
+}
+
 template <int BN, int MODE, bool PERM, int BITS>
 int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
                 const uint32_t* zeros, int M, int N, int K, int gs, void* out, int ldo,
-                const float* yref, int ldy, cudaStream_t st) {
+                const float* yref, int ldy, cudaStream_t st, int splits = 1, int kps = 0,
+                float* part = nullptr) {
   using C = Cfg<BN, MODE, BITS>;
+  if (kps == 0) kps = K / BK;
   static bool attr_set = false;
   if (!attr_set) {
     AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE, PERM, BITS>,
@@ -494,8 +542,8 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
     AWQ_CUDA_TRY(cudaGetDevice(&dev));
     AWQ_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   }
-  const int tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
-  cfg.gridDim = dim3(tiles < sms ? tiles : sms, 1, 1);
+  const int items = ((N + BM - 1) / BM) * ((M + BN - 1) / BN) * splits;
+  cfg.gridDim = dim3(items < sms ? items : sms, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
@@ -504,31 +552,41 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM, BITS>, tb, ta, scales, zeros, M, N, K, gs, out,
-                                  ldo, yref, ldy));
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM, BITS>, tb, ta, scales, zeros,
+                                  M, N, K, gs, out, ldo, yref, ldy, splits, kps, part));
+  if (splits > 1) {
+    // ldo == N for the split-K plan: the partials and Y are dense [M][N]
+    const int64_t mn4 = static_cast<int64_t>(M) * N / 4;
+    cudaLaunchConfig_t rc = cfg;
+    rc.gridDim = dim3(static_cast<unsigned>(sms * 4), 1, 1);
+    rc.blockDim = dim3(256, 1, 1);
+    rc.dynamicSmemBytes = 0;
+    AWQ_CUDA_TRY(cudaLaunchKernelEx(&rc, splitk_reduce_kernel, static_cast<const float*>(part),
+                                    splits, mn4, static_cast<__half*>(out)));
+  }
   return AWQ_OK;
 }
 
 template <int MODE, bool PERM, int BITS>
 int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
                 const uint32_t* zeros, int M, int N, int K, int gs, void* out, int ldo,
-                const float* yref, int ldy, cudaStream_t st) {
+                const float* yref, int ldy, cudaStream_t st, int splits, int kps, float* part) {
   switch (bn) {
     case 16:
       return launch_tile<16, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
-                                               ldy, st);
+                                               ldy, st, splits, kps, part);
     case 32:
       return launch_tile<32, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
-                                               ldy, st);
+                                               ldy, st, splits, kps, part);
     case 64:
       return launch_tile<64, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
-                                               ldy, st);
+                                               ldy, st, splits, kps, part);
     case 128:
       return launch_tile<128, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
-                                                yref, ldy, st);
+                                                yref, ldy, st, splits, kps, part);
     default:
       return launch_tile<256, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
-                                                yref, ldy, st);
+                                                yref, ldy, st, splits, kps, part);
   }
 }
 
@@ -541,7 +599,63 @@ int pick_bn(int M, int mode) {
   return 256;
 }
 
+int sm_count() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+  }
+  return sms;
+}
+
 }  // namespace
+
+// Token-tile width and split-K for one launch.  The tile is the smallest of
+// 16..256 tokens that holds M; split-K comes from a cost model in SM cycles:
+// a k-block of a work item costs max(2 BN, 208) cycles (tensor-core work of a
+// 128 x BN x 64 MMA, or the 8 dequantization warps' share of 1024 packed
+// words, whichever is larger); items run in rounds of one per SM; a split-K
+// plan pays the fp32 partial sums written and read back (8 bytes per output
+// per split at ~3250 bytes per cycle) and a second launch.  Only the plain
+// fp16 output takes split-K (at most 8 splits of >= 8 k-blocks each).
+GemmPlan plan_gemm(int M, int N, int K, int mode) {
+  const int sms = sm_count();
+  const int nk = K / BK;
+  const int n_tiles = (N + BM - 1) / BM;
+  GemmPlan best{pick_bn(M, mode), 1, nk};
+  double best_t = -1.0;
+  {
+    // above 128 tokens the widest tile (measured: 128-token tiles lose more
+    // to per-stage overheads than they win back on wave quantization)
+    const int bn = pick_bn(M, mode);
+    const int tiles = n_tiles * ((M + bn - 1) / bn);
+    const double c = 2.0 * bn > 208.0 ? 2.0 * bn : 208.0;
+    const int max_s = mode == kGemmOutF16 ? 8 : 1;
+    for (int s = 1; s <= max_s; ++s) {
+      const int kps = ((nk + s - 1) / s + 1) & ~1;
+      if (s > 1 && kps < 8) break;
+      const int s_eff = (nk + kps - 1) / kps;
+      if (s_eff != s) continue;
+      const int items = tiles * s;
+      const int rounds = (items + sms - 1) / sms;
+      double t = static_cast<double>(rounds) * kps * c;
+      if (s > 1) t += 8.0 * s * static_cast<double>(M) * N / 3250.0 + 2000.0;
+      if (best_t < 0 || t < best_t) {
+        best_t = t;
+        best = GemmPlan{bn, s, kps};
+      }
+    }
+  }
+  if (best.splits == 1) best.kps = nk;
+  return best;
+}
+
+size_t gemm_partial_bytes(int M, int N, int K) {
+  const GemmPlan p = plan_gemm(M, N, K, kGemmOutF16);
+  return p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 0;
+}
 
 int gemm_sqerr_slots(int M) { return (M + 255) / 256; }
 
@@ -572,21 +686,21 @@ template <int BITS>
 int launch_gemm_bits(int mode, int bn, const CUtensorMap& tb, const CUtensorMap& ta,
                      bool xt_permuted, int M, const __half* scales, const uint32_t* zeros, int N,
                      int K, int gs, void* out, int ldo, const float* yref, int ldy,
-                     cudaStream_t st) {
+                     cudaStream_t st, int splits, int kps, float* part) {
   switch (mode) {
     case kGemmOutF16:
       if (xt_permuted)
         return dispatch_bn<kGemmOutF16, true, BITS>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                    ldo, yref, ldy, st);
+                                                    ldo, yref, ldy, st, splits, kps, part);
       return dispatch_bn<kGemmOutF16, false, BITS>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                   ldo, yref, ldy, st);
+                                                   ldo, yref, ldy, st, splits, kps, part);
     case kGemmSiluF16:
       if constexpr (BITS == 4) {
         if (xt_permuted)
           return dispatch_bn<kGemmSiluF16, true, 4>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                    ldo, yref, ldy, st);
+                                                    ldo, yref, ldy, st, 1, 0, nullptr);
         return dispatch_bn<kGemmSiluF16, false, 4>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                   ldo, yref, ldy, st);
+                                                   ldo, yref, ldy, st, 1, 0, nullptr);
       }
       set_error("the fused gate/up layer takes 4-bit codes");
       return AWQ_ERR_UNSUPPORTED;
@@ -608,12 +722,20 @@ int launch_gemm_bits(int mode, int bn, const CUtensorMap& tb, const CUtensorMap&
 int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
                 const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
                 void* out, int ldo, const float* yref, int ldy, cudaStream_t st, int w_bit,
-                int group) {
+                int group, float* part, size_t part_bytes) {
   if ((w_bit != 4 && w_bit != 8) || (group != 32 && group != 64 && group != 128)) {
     set_error("awq_gemm: w_bit = %d, group = %d is not supported", w_bit, group);
     return AWQ_ERR_UNSUPPORTED;
   }
-  const int bn = pick_bn(M, mode);
+  GemmPlan plan = plan_gemm(M, N, K, mode);
+  // split-K needs the partial sums' workspace and a dense [M][N] output
+  if (plan.splits > 1 &&
+      (!part || part_bytes < static_cast<size_t>(plan.splits) * M * N * sizeof(float) ||
+       ldo != N || !aligned16(part))) {
+    plan.splits = 1;
+    plan.kps = K / BK;
+  }
+  const int bn = plan.bn;
   CUtensorMap tb, ta;
   int rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xt, K, M, static_cast<uint64_t>(K) * 2,
                         BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -634,9 +756,9 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
   if (rc != AWQ_OK) return rc;
   if (w_bit == 8)
     return launch_gemm_bits<8>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
-                               ldo, yref, ldy, st);
+                               ldo, yref, ldy, st, plan.splits, plan.kps, part);
   return launch_gemm_bits<4>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
-                             ldo, yref, ldy, st);
+                             ldo, yref, ldy, st, plan.splits, plan.kps, part);
 }
 
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags) {

@@ -48,10 +48,19 @@ int launch_prescale(const __half* X, const float* inv_s, int64_t M, int K, __hal
 //   kGemmDenseF32: out = fp32 Xt * Wd^T, Wd fp16 [N][K] dense
 //   kGemmSiluF16 : the N weight rows stack N/2 gate rows over N/2 up rows;
 //                  out = fp16 silu(gate) * up, [M][ldo] with N/2 columns
+// part/part_bytes: workspace for split-K partial sums (kGemmOutF16 only; with
+// too little or none the launch runs without split-K).
 int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
                 const __half* scales, const uint32_t* zeros, const __half* Wd, int N, int K,
                 void* out, int ldo, const float* yref, int ldy, cudaStream_t st, int w_bit = 4,
-                int group = 128);
+                int group = 128, float* part = nullptr, size_t part_bytes = 0);
+struct GemmPlan {
+  int bn;       // token-tile width
+  int splits;   // split-K factor
+  int kps;      // k-blocks (64 channels) per split
+};
+GemmPlan plan_gemm(int M, int N, int K, int mode);
+size_t gemm_partial_bytes(int M, int N, int K);   // split-K workspace of the plain matmul
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
 
