@@ -10,4 +10,5 @@ from .awq_oracle import (GROUP, W_BIT, QMAX, N_GRID, TOL_REL, MSE_REL,  # noqa: 
                          awq_pack, dequant, scaled_activations, linear,
                          ulp_fp16, tolerance, row_errors, search, gram,
                          row_errors_gram, SILU_LIP, silu, silu_mul_linear,
-                         fold_inv_scales)
+                         fold_inv_scales, CLIP_MIN, clip_ratios, quantize_clipped,
+                         group_gram, clip_search)

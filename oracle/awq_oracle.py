@@ -385,3 +385,92 @@ def fold_inv_scales(W16, inv_s):
     W2 = W.reshape(shape[0], -1).astype(np.float32)
     out = (W2 * np.asarray(inv_s, dtype=np.float32)[:, None]).astype(np.float32)
     return out.astype(np.float16).reshape(shape)
+
+
+# ------------------------------------------------------- weight clipping
+# The pages name a clipping parameter (``clip_steps``, suggested 200, in the
+# troubleshooting section of "AWQ量化实战..." §5.1) and nothing more.
+# READING: after the scale search, each group's range [min, max] of the
+# scaled weights may shrink to [r min, r max] with r on a grid
+# r_i = 1 - 0.5 i / n (i = 0 .. n-1, n = the number of clip steps); the
+# group is quantized from the shrunk range (codes clamp, which clips), and
+# the ratio that minimises the group's output error on the calibration
+# tokens, e = sum_t (sum_k x~_tk (w^_k - w'_k))^2 = d^T H_g d with
+# H_g = X~_g^T X~_g, is kept (ties: the smallest i, the least clipping).
+CLIP_MIN = 0.5
+
+
+def clip_ratios(n_clip: int) -> np.ndarray:
+    """``r_i = fp32(1 - 0.5 i / n)``, i = 0..n-1."""
+    return (1.0 - CLIP_MIN * np.arange(n_clip, dtype=np.float64) / n_clip).astype(np.float32)
+
+
+def quantize_clipped(W16, s_c, ratio_idx, n_clip, group=GROUP, w_bit=W_BIT, zero_point=True):
+    """:func:`quantize` with each group's range shrunk by ``r[ratio_idx[n, g]]``.
+
+    The shrunk range is ``[fp32(r mn), fp32(r mx)]`` (symmetric: ``r max|w'|``);
+    step, zero point and codes follow from it by the same rules (codes clamp,
+    which clips the weights outside the range).  ``ratio_idx`` all 0 is
+    :func:`quantize` exactly.
+    """
+    qmax = (1 << w_bit) - 1
+    W = np.asarray(W16, dtype=np.float16).astype(np.float32)
+    N, K = W.shape
+    if s_c is not None:
+        W = (W * np.asarray(s_c, dtype=np.float32)[None, :]).astype(np.float32)
+    G = K // group
+    Wg = W.reshape(N, G, group)
+    r = clip_ratios(n_clip)[np.asarray(ratio_idx, dtype=np.int64)]   # fp32 [N, G]
+    if zero_point:
+        mn = (Wg.min(axis=2) * r).astype(np.float32)
+        mx = (Wg.max(axis=2) * r).astype(np.float32)
+        s32 = ((mx - mn) / np.float32(qmax)).astype(np.float32)
+    else:
+        h = 1 << (w_bit - 1)
+        s32 = ((np.abs(Wg).max(axis=2) * r).astype(np.float32) / np.float32(h - 1)).astype(np.float32)
+    s32 = np.minimum(np.maximum(s32, S_MIN), S_MAX)
+    s16 = s32.astype(np.float16)
+    s = s16.astype(np.float32)
+    if zero_point:
+        z = np.clip(np.rint((-mn) / s), 0, qmax).astype(np.float32)
+        q = np.clip(np.rint(Wg / s[:, :, None]) + z[:, :, None], 0, qmax)
+    else:
+        z = np.full((N, G), float(h), dtype=np.float32)
+        q = np.clip(np.rint(Wg / s[:, :, None]), -h, h - 1) + h
+    return (q.reshape(N, K).astype(np.uint8), z.astype(np.uint8), s16)
+
+
+def group_gram(X16, inv_s, group=GROUP, token_chunk=4096):
+    """``H_g = X~_g^T X~_g`` for every group g of input channels (fp64
+    [G, group, group]), with ``x~ = fp32(x) * inv_s`` as in the layer."""
+    X16 = np.asarray(X16, dtype=np.float16)
+    T, K = X16.shape
+    G = K // group
+    H = np.zeros((G, group, group), dtype=np.float64)
+    for t0 in range(0, T, token_chunk):
+        xt = scaled_activations(X16[t0:t0 + token_chunk], inv_s).astype(np.float64)
+        xg = xt.reshape(-1, G, group)
+        H += np.einsum("tgi,tgj->gij", xg, xg)
+    return H
+
+
+def clip_search(X16, W16, s_c, inv_s, n_clip=20, group=GROUP, w_bit=W_BIT, zero_point=True):
+    """Per-group clipping ratio by the group's output error (see the READING
+    above).  Returns ``(ratio_idx uint8 [N, G], err fp64 [N, G, n_clip])``."""
+    W16 = np.asarray(W16, dtype=np.float16)
+    N, K = W16.shape
+    G = K // group
+    H = group_gram(X16, inv_s, group)
+    Wp = W16.astype(np.float32)
+    if s_c is not None:
+        Wp = (Wp * np.asarray(s_c, dtype=np.float32)[None, :]).astype(np.float32)
+    Wp = Wp.reshape(N, G, group).astype(np.float64)
+    err = np.empty((N, G, n_clip), dtype=np.float64)
+    for i in range(n_clip):
+        idx = np.full((N, G), i, dtype=np.int64)
+        q, z, s16 = quantize_clipped(W16, s_c, idx, n_clip, group, w_bit, zero_point)
+        wq = ((q.reshape(N, G, group).astype(np.float64) - z[:, :, None]) *
+              s16.astype(np.float64)[:, :, None])
+        d = wq - Wp
+        err[:, :, i] = np.einsum("ngi,gij,ngj->ng", d, H, d)
+    return np.argmin(err, axis=2).astype(np.uint8), err
