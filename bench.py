@@ -504,6 +504,33 @@ def sweep_70b(awq, torch, hbm, pk, reps=5):
                     "decode GB/s, exact for the tensor-bound M", "layers": out}
 
 
+def clip_run(awq, torch, model=MODEL, name="qkv", T=4096, n_clip=20):
+    """Wall time of the per-group clipping search on one layer: the group Gram
+    matrices over T calibration tokens and n_clip candidate ratios per group
+    (each a quadratic form d^T H_g d of 128 x 128 fp32 multiply-adds)."""
+    dev = torch.device("cuda")
+    K, N, lid = awq_inputs.layer(model, name)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + lid)
+    W = (torch.randn((N, K), generator=gen, device=dev) * 0.02).half()
+    gen.manual_seed(2000 + lid)
+    X = torch.randn((T, K), generator=gen, device=dev).half()
+    s_c = torch.ones(K, dtype=torch.float32, device=dev)
+    awq.clip_search(X[:256].contiguous(), W[:64].contiguous(), s_c, s_c, n_clip)   # warm-up
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    idx = awq.clip_search(X, W, s_c, s_c, n_clip)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    fma = float(N) * K * 128 * n_clip + float(T) * K * 128
+    clipped = float((idx > 0).float().mean().item())
+    del X, W
+    return {"layer": f"{model}:{name} {K}->{N}", "calib_tokens": T, "n_clip": n_clip,
+            "seconds": round(dt, 3), "fp32_tflops": round(2 * fma / dt / 1e12, 2),
+            "groups_clipped": round(clipped, 3),
+            "includes": "group Gram matrices, n_clip quadratic forms per group, argmin"}
+
+
 def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
     """Wall time of awq_search_scales on one layer (20 alphas) and the
     TFLOP/s of its tensor-core work (Y_ref once + 20 squared-error passes)."""
@@ -545,6 +572,7 @@ def main():
     ap.add_argument("--no-70b", action="store_true", help="skip the 70B-shape GEMV figures")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused gate/up figures")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 70B token-count sweep")
+    ap.add_argument("--no-clip", action="store_true", help="skip the clipping-search timing")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the quantization-variant figures")
     ap.add_argument("--only-gemm", default=None, metavar="MODEL:LAYER:M",
@@ -689,6 +717,7 @@ def main():
     fused = None if args.no_fused else fused_gate_up(awq, torch, hbm, pk)
     var = None if args.no_variants else variants(awq, torch, hbm, pk)
     sweep = None if args.no_sweep else sweep_70b(awq, torch, hbm, pk)
+    clip = None if args.no_clip else clip_run(awq, torch)
     search = None if args.no_search else search_run(awq, torch)
     awq.check_device_error()
 
@@ -727,6 +756,7 @@ def main():
         "fused_gate_up": fused,
         "variants": var,
         "sweep_70b": sweep,
+        "clip": clip,
         "gemm_prefill": gemm,
         "search": search,
     }

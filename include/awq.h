@@ -221,6 +221,32 @@ AWQ_API int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qwei
 AWQ_API int awq_fold_inv_scales(const uint16_t* W, int64_t rows, int64_t cols,
                         const float* inv_s, uint16_t* out, void* stream);
 
+/* ---------------------------------------------------- weight clipping
+ * ("AWQ量化实战" §5.1 names a clipping parameter, clip_steps, suggested 200,
+ * and nothing more.)  Library reading: after the scale search, each group's
+ * range [min, max] of the scaled weights W diag(s_c) may shrink to
+ * [r min, r max] (symmetric: r max|w'|) with r_i = fp32(1 - 0.5 i / n_clip),
+ * i = 0 .. n_clip-1; the group is quantized from the shrunk range (codes clamp,
+ * which clips) and the ratio with the smallest output error on the calibration
+ * tokens, d^T H_g d with d = w^ - w' and H_g = X~_g^T X~_g (x~ = x * inv_s),
+ * is kept; ties go to the least clipping (smallest i).
+ * awq_clip_search: X_cal fp16 [T][K]; W fp16 [N][K]; s_c, inv_s fp32 [K] or
+ * NULL (the scales of the chosen alpha); clip_idx out uint8 [N][G] device;
+ * err_out fp32 [N][G][n_clip] device or NULL (every candidate's error, fp32
+ * sums); 1 <= n_clip <= 200. Workspace: awq_clip_search_workspace_size bytes
+ * (the group Gram matrices and their per-chunk partial sums).
+ * awq_pack_clipped: awq_pack with each group's range shrunk by
+ * clip_idx[n][g] (n_clip as in the search); clip_idx all 0 is awq_pack. */
+AWQ_API size_t awq_clip_search_workspace_size(int64_t T, int32_t K, const awq_config* cfg);
+AWQ_API int awq_clip_search(const uint16_t* X_cal, int64_t T, const uint16_t* W,
+                    int32_t N, int32_t K, const float* s_c, const float* inv_s,
+                    const awq_config* cfg, int32_t n_clip, void* workspace,
+                    size_t ws_bytes, uint8_t* clip_idx, float* err_out, void* stream);
+AWQ_API int awq_pack_clipped(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
+                     const awq_config* cfg, const uint8_t* clip_idx, int32_t n_clip,
+                     uint32_t* qweight, uint16_t* scales, uint32_t* zeros,
+                     void* stream);
+
 /* ------------------------------------------------------------ scale search
  * The activation-aware grid search ("AWQ量化实战" §2.2, §3.3 第四步, §5.1: one
  * coefficient per layer, no backpropagation): a = absmean(X_cal); for each

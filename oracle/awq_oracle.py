@@ -449,8 +449,9 @@ def group_gram(X16, inv_s, group=GROUP, token_chunk=4096):
     H = np.zeros((G, group, group), dtype=np.float64)
     for t0 in range(0, T, token_chunk):
         xt = scaled_activations(X16[t0:t0 + token_chunk], inv_s).astype(np.float64)
-        xg = xt.reshape(-1, G, group)
-        H += np.einsum("tgi,tgj->gij", xg, xg)
+        for g in range(G):
+            xg = xt[:, g * group:(g + 1) * group]
+            H[g] += xg.T @ xg
     return H
 
 

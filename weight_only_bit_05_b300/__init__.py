@@ -28,7 +28,7 @@ import torch
 
 __all__ = ["lib", "LIB_PATH", "AwqError", "exported_symbols", "absmean", "channel_scales", "pack",
            "gemv", "gemm", "search", "check_device_error", "gemm_workspace_bytes",
-           "gemv_silu_mul", "gemm_silu_mul", "fold_inv_scales"]
+           "gemv_silu_mul", "gemm_silu_mul", "fold_inv_scales", "clip_search", "pack_clipped"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libawq.so")
@@ -65,6 +65,11 @@ _SIGS = {
     "awq_gemm_ex": (ctypes.c_int, [ctypes.POINTER(AwqConfig), _p, _i32, _p, _p, _p, _p, _i32,
                                    _i32, _p, _p, _sz, _p]),
     "awq_fold_inv_scales": (ctypes.c_int, [_p, _i64, _i64, _p, _p, _p]),
+    "awq_clip_search_workspace_size": (_sz, [_i64, _i32, ctypes.POINTER(AwqConfig)]),
+    "awq_clip_search": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, _p, _p,
+                                       ctypes.POINTER(AwqConfig), _i32, _p, _sz, _p, _p, _p]),
+    "awq_pack_clipped": (ctypes.c_int, [_p, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p, _i32,
+                                        _p, _p, _p, _p]),
     "awq_search_workspace_size": (_sz, [_i64, _i32, _i32]),
     "awq_search_scales": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p,
                                          _sz, _p, _p, ctypes.POINTER(ctypes.c_int32),
@@ -244,6 +249,47 @@ def fold_inv_scales(W: torch.Tensor, inv_s: torch.Tensor, out=None):
     Y = out if out is not None else torch.empty_like(W)
     _check(lib.awq_fold_inv_scales(_ptr(W), rows, cols, _ptr(inv_s), _ptr(Y), _stream()))
     return Y
+
+
+def clip_search(X_cal: torch.Tensor, W: torch.Tensor, s_c=None, inv_s=None, n_clip: int = 20,
+                w_bit: int = 4, group: int = 128, zero_point: bool = True, err: bool = False):
+    """Per-group clipping ratio index (uint8 [N][K/group]) and, with err=True,
+    every candidate's error (fp32 [N][G][n_clip])."""
+    _dev(X_cal, torch.float16, "X_cal")
+    _dev(W, torch.float16, "W")
+    for t, nm in ((s_c, "s_c"), (inv_s, "inv_s")):
+        if t is not None:
+            _dev(t, torch.float32, nm)
+    T, K = X_cal.shape
+    N = W.shape[0]
+    G = K // group
+    cfg = _cfg(w_bit, group, zero_point)
+    ws = torch.empty(lib.awq_clip_search_workspace_size(T, K, ctypes.byref(cfg)),
+                     dtype=torch.uint8, device=W.device)
+    idx = torch.empty((N, G), dtype=torch.uint8, device=W.device)
+    e = torch.empty((N, G, n_clip), dtype=torch.float32, device=W.device) if err else None
+    _check(lib.awq_clip_search(_ptr(X_cal), T, _ptr(W), N, K, _ptr(s_c), _ptr(inv_s),
+                               ctypes.byref(cfg), n_clip, _ptr(ws), ws.numel(), _ptr(idx), _ptr(e),
+                               _stream()))
+    return (idx, e) if err else idx
+
+
+def pack_clipped(W: torch.Tensor, s_c, clip_idx: torch.Tensor, n_clip: int = 20, w_bit: int = 4,
+                 group: int = 128, zero_point: bool = True):
+    _dev(W, torch.float16, "W")
+    if s_c is not None:
+        _dev(s_c, torch.float32, "s_c")
+    _dev(clip_idx, torch.uint8, "clip_idx")
+    N, K = W.shape
+    c = 32 // w_bit
+    G = K // group
+    qweight = torch.empty((N, K // c), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((N, (G + c - 1) // c), dtype=torch.int32, device=W.device)
+    cfg = _cfg(w_bit, group, zero_point)
+    _check(lib.awq_pack_clipped(_ptr(W), _ptr(s_c), N, K, ctypes.byref(cfg), _ptr(clip_idx),
+                                n_clip, _ptr(qweight), _ptr(scales), _ptr(zeros), _stream()))
+    return qweight, scales, zeros
 
 
 def search(X_cal: torch.Tensor, W: torch.Tensor, n_grid: int = 20, row_err: bool = False,

@@ -270,6 +270,68 @@ size_t xt_bytes(int32_t M, int32_t K) {
 }
 }  // namespace
 
+size_t awq_clip_search_workspace_size(int64_t T, int32_t K, const awq_config* cfg) {
+  const awq_config c = cfg ? *cfg : awq_default_config();
+  if (T <= 0 || K <= 0 || (c.group != 128 && c.group != 64 && c.group != 32) ||
+      K % c.group != 0)
+    return 0;
+  return clip_workspace_size(T, K, c.group);
+}
+
+int awq_clip_search(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32_t N, int32_t K,
+                    const float* s_c, const float* inv_s, const awq_config* cfg, int32_t n_clip,
+                    void* workspace, size_t ws_bytes, uint8_t* clip_idx, float* err_out,
+                    void* stream) {
+  AWQ_TRY(check_cfg(cfg));
+  const awq_config c = cfg ? *cfg : awq_default_config();
+  AWQ_TRY(check_kn(N, K));
+  if (T < 1) {
+    set_error("awq_clip_search: T = %lld must be >= 1", static_cast<long long>(T));
+    return AWQ_ERR_SHAPE;
+  }
+  if (n_clip < 1 || n_clip > 200) {
+    set_error("awq_clip_search: n_clip = %d must be in [1, 200]", n_clip);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(X_cal, "X_cal"));
+  AWQ_TRY(check_ptr(W, "W"));
+  AWQ_TRY(check_opt_ptr(s_c, "s_c"));
+  AWQ_TRY(check_opt_ptr(inv_s, "inv_s"));
+  AWQ_TRY(check_ptr(clip_idx, "clip_idx"));
+  AWQ_TRY(check_opt_ptr(err_out, "err_out"));
+  if (!workspace || !aligned16(workspace) ||
+      ws_bytes < awq_clip_search_workspace_size(T, K, cfg)) {
+    set_error("awq_clip_search: workspace must be 16-B aligned and >= %zu bytes",
+              awq_clip_search_workspace_size(T, K, cfg));
+    return AWQ_ERR_WORKSPACE;
+  }
+  return launch_clip_search(reinterpret_cast<const __half*>(X_cal), T,
+                            reinterpret_cast<const __half*>(W), N, K, s_c, inv_s, c.w_bit,
+                            c.group, c.zero_point != 0, n_clip, workspace, clip_idx, err_out,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int awq_pack_clipped(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
+                     const awq_config* cfg, const uint8_t* clip_idx, int32_t n_clip,
+                     uint32_t* qweight, uint16_t* scales, uint32_t* zeros, void* stream) {
+  AWQ_TRY(check_cfg(cfg));
+  AWQ_TRY(check_kn(N, K));
+  if (n_clip < 1 || n_clip > 200) {
+    set_error("awq_pack_clipped: n_clip = %d must be in [1, 200]", n_clip);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(W, "W"));
+  AWQ_TRY(check_opt_ptr(s_c, "s_c"));
+  AWQ_TRY(check_ptr(clip_idx, "clip_idx"));
+  AWQ_TRY(check_ptr(qweight, "qweight"));
+  AWQ_TRY(check_ptr(scales, "scales"));
+  AWQ_TRY(check_ptr(zeros, "zeros"));
+  const awq_config c = cfg ? *cfg : awq_default_config();
+  return launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
+                     reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream),
+                     c.w_bit, c.group, c.zero_point != 0, clip_idx, n_clip);
+}
+
 size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {
   if (M <= 0 || K <= 0 || N <= 0 || K % kGroup != 0) return 0;
   return xt_bytes(M, K) + gemm_partial_bytes(M, N, K);

@@ -15,9 +15,19 @@ int launch_channel_scales(const float* a, int K, double alpha, float* s_c, float
 // awq_pack.cu
 // w_bit 4 or 8, group 128/64/32, zero_point on (asymmetric) or off
 // (symmetric: codes offset by 2^(w_bit-1), stored as the zero point).
+// clip_idx (optional, uint8 [N][G]) shrinks each group's range by the ratio
+// 1 - 0.5 i / n_clip before quantization.
 int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweight,
                 __half* scales, uint32_t* zeros, cudaStream_t st, int w_bit = 4,
-                int group = 128, bool zero_point = true);
+                int group = 128, bool zero_point = true, const uint8_t* clip_idx = nullptr,
+                int n_clip = 1);
+
+// awq_clip.cu
+size_t clip_workspace_size(int64_t T, int K, int group);
+int launch_clip_search(const __half* X, int64_t T, const __half* W, int N, int K,
+                       const float* s_c, const float* inv_s, int w_bit, int group,
+                       bool zero_point, int n_clip, void* ws, uint8_t* clip_idx, float* err,
+                       cudaStream_t st);
 
 // awq_gemv.cu
 // silu_mul: the weight's N rows are I = N/2 gate rows over I up rows and Y

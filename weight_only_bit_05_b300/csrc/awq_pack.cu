@@ -18,11 +18,22 @@
 namespace awq {
 namespace {
 
+// Shrink ratio i of an n-point clipping grid: fp32(1 - 0.5 i / n), the fp64
+// operations in the order of the definition.
+__device__ __forceinline__ float clip_ratio(int i, int n) {
+  return __double2float_rn(__dsub_rn(1.0, __ddiv_rn(__dmul_rn(0.5, static_cast<double>(i)),
+                                                    static_cast<double>(n))));
+}
+
+// clip_idx (optional, uint8 [N][G]): the group's range is shrunk by
+// clip_ratio(clip_idx[n][g], n_clip) before its step and zero point are set;
+// the codes then clamp, which clips the weights outside the shrunk range.
 template <int BITS, int GS, bool ZP>
 __global__ void __launch_bounds__(256)
     quant_pack_kernel(const __half* __restrict__ W, const float* __restrict__ s_c, int N, int K,
                       uint32_t* __restrict__ qweight, __half* __restrict__ scales,
-                      uint32_t* __restrict__ zeros) {
+                      uint32_t* __restrict__ zeros, const uint8_t* __restrict__ clip_idx,
+                      int n_clip) {
   constexpr int kPerWord = 32 / BITS;             // codes per packed word
   constexpr int kQmax = (1 << BITS) - 1;
   constexpr int kHalf = 1 << (BITS - 1);
@@ -81,8 +92,15 @@ __global__ void __launch_bounds__(256)
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
 
+  float amax = fmaxf(fabsf(mn), fabsf(mx));
+  if (clip_idx && valid) {
+    const float r = clip_ratio(clip_idx[static_cast<size_t>(n) * G + k0 / GS], n_clip);
+    mn = __fmul_rn(mn, r);
+    mx = __fmul_rn(mx, r);
+    amax = __fmul_rn(amax, r);
+  }
   float s32 = ZP ? __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kQmax))
-                 : __fdiv_rn(fmaxf(fabsf(mn), fabsf(mx)), static_cast<float>(kHalf - 1));
+                 : __fdiv_rn(amax, static_cast<float>(kHalf - 1));
   s32 = fminf(fmaxf(s32, 6.103515625e-05f), 65504.0f);   // [2^-14, 65504]
   const __half s16 = __float2half_rn(s32);
   const float s = __half2float(s16);
@@ -131,14 +149,14 @@ __global__ void __launch_bounds__(256)
 
 int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweight,
                 __half* scales, uint32_t* zeros, cudaStream_t st, int w_bit, int group,
-                bool zero_point) {
+                bool zero_point, const uint8_t* clip_idx, int n_clip) {
   const int units = (K + 1023) / 1024;
   const int64_t warps = static_cast<int64_t>(N) * units;
   const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
 #define AWQ_PACK_CASE(B, GS, ZP)                                                         \
   if (w_bit == B && group == GS && zero_point == ZP) {                                   \
     quant_pack_kernel<B, GS, ZP><<<blocks, 256, 0, st>>>(W, s_c, N, K, qweight, scales, \
-                                                         zeros);                        \
+                                                         zeros, clip_idx, n_clip);      \
     AWQ_CUDA_TRY_LAUNCH("quant_pack_kernel");                                            \
     return AWQ_OK;                                                                       \
   }
