@@ -559,6 +559,18 @@ def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
                                                "GEMM, reductions), Y_ref GEMM, host argmin"}
 
 
+def replica_value(torch, ms_local, world, step_bytes, steps, device):
+    """Whole-job throughput of N independent replicas (weak scaling, no data
+    collective): every rank processed ``step_bytes`` per step, the job time
+    is the slowest rank's (a MAX all-reduce of the timings), so the value is
+    world * step_bytes * steps / max_ms.  Returns (max_ms, GB/s)."""
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, world * step_bytes * steps / (ms / 1000) / 1e9
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,12 +673,8 @@ def main():
         e1.record()
         torch.cuda.synchronize()
     barrier()
-    ms_total = e0.elapsed_time(e1)
-    t = torch.tensor([ms_total], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_total = float(t.item())
-    value = world * step_bytes * args.steps / (ms_total / 1000) / 1e9
+    ms_total, value = replica_value(torch, e0.elapsed_time(e1), world, step_bytes, args.steps,
+                                    "cuda")
 
     # GEMV kernel timing, per shape: graph of that shape's launches over all layers
     per_shape = {}
