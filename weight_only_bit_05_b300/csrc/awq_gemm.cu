@@ -341,7 +341,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = MODE == kGemmSiluF16 ? (v >> 1) + (v & 1) * (N / 2) : v;
         const bool row_ok = MODE == kGemmSiluF16 ? (v >> 1) < N / 2 : v < N;
         const int raw_r = MODE == kGemmSiluF16 ? (r >> 1) + (r & 1) * (BM / 2) : r;
-        // steps and zero points of this thread's next kSzAhead groups, oldest first
+        // Steps and zero points.  When every row's groups come in whole
+        // blocks of 8 (G % 8 == 0) and this thread meets every group, they
+        // are read 8 at a time (one 16-byte load of steps, one or two words of
+        // zero points) into two register blocks, the next block 8 groups ahead
+        // of use; otherwise one group at a time, kSzAhead groups ahead.
+        const bool blocks8 = (G % 8 == 0) && gstride == 1;
+        uint4 sblk[2];
+        uint32_t zblk[2][2];
+        auto load_blk = [&](int b, int slot) {
+          if (row_ok && 8 * b < G) {
+            sblk[slot] = __ldg(reinterpret_cast<const uint4*>(scales + static_cast<size_t>(n) * G + 8 * b));
+            const uint32_t* zp = zeros + static_cast<size_t>(n) * ZW + (8 * b) / PW;
+            zblk[slot][0] = __ldg(zp);
+            zblk[slot][1] = PW == 4 ? __ldg(zp + 1) : 0u;
+          } else {
+            sblk[slot] = make_uint4(0, 0, 0, 0);
+            zblk[slot][0] = zblk[slot][1] = 0u;
+          }
+        };
         __half sq[kSzAhead];
         uint32_t zq[kSzAhead];
         auto load_sz = [&](int i, __half& sv, uint32_t& zv) {
@@ -354,23 +372,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             zv = 0;
           }
         };
+        const int gi0 = kb0 >> kb_shift;
+        if (blocks8) {
+          load_blk(gi0 >> 3, 0);
+          load_blk((gi0 >> 3) + 1, 1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < kSzAhead; ++i) load_sz((kb0 >> kb_shift) + i, sq[i], zq[i]);
+          for (int i = 0; i < kSzAhead; ++i) load_sz(gi0 + i, sq[i], zq[i]);
+        }
         uint32_t zbe = 0x64006400u, zbo = 0x54005400u;
         __half2 s2 = __half2half2(__ushort_as_half(0));
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
           if ((kb & kb_mask) == 0) {
             const int gi = kb >> kb_shift;   // this thread's group counter
-            s2 = __half2half2(sq[0]);
-            zbe = (0x6400u | zq[0]) * 0x00010001u;          // (1024 + z, 1024 + z)
-            zbo = (0x5400u | (zq[0] << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
+            uint32_t zc;
+            if (blocks8) {
+              const int j = gi & 7;
+              if (j == 0 && gi != gi0) {     // block done: the next one becomes current
+                sblk[0] = sblk[1];
+                zblk[0][0] = zblk[1][0];
+                zblk[0][1] = zblk[1][1];
+                load_blk((gi >> 3) + 1, 1);
+              }
+              const uint32_t sw = (j >> 1) == 0 ? sblk[0].x : (j >> 1) == 1 ? sblk[0].y
+                                : (j >> 1) == 2 ? sblk[0].z : sblk[0].w;
+              s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sw >> (16 * (j & 1)))));
+              zc = PW == 8 ? (zblk[0][0] >> (4 * j)) & QMASK
+                           : (((j >> 2) == 0 ? zblk[0][0] : zblk[0][1]) >> (8 * (j & 3))) & QMASK;
+            } else {
+              s2 = __half2half2(sq[0]);
+              zc = zq[0];
 #pragma unroll
-            for (int i = 0; i + 1 < kSzAhead; ++i) {
-              sq[i] = sq[i + 1];
-              zq[i] = zq[i + 1];
+              for (int i = 0; i + 1 < kSzAhead; ++i) {
+                sq[i] = sq[i + 1];
+                zq[i] = zq[i + 1];
+              }
+              load_sz(gi + kSzAhead, sq[kSzAhead - 1], zq[kSzAhead - 1]);
             }
-            load_sz(gi + kSzAhead, sq[kSzAhead - 1], zq[kSzAhead - 1]);
+            zbe = (0x6400u | zc) * 0x00010001u;          // (1024 + z, 1024 + z)
+            zbo = (0x5400u | (zc << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
           }
           if (!wait_or_abort(full + s, (it / S) & 1, ab, 4u)) {
             ok = false;
