@@ -457,6 +457,59 @@ def variants(awq, torch, hbm, pk, reps=20):
     return out
 
 
+BATCHED_M = (8, 32, 128)
+
+
+def batched_7b(awq, torch, hbm, pk, reps=10):
+    """The Llama-2-7B shapes as batched decode, M = 8 / 32 / 128: awq_gemv at
+    M = 8 and awq_gemm at every M, over rotating weight copies (weights do
+    not stay in L2); GB/s of the algorithmic bytes and TFLOP/s of 2 M N K."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    out = {}
+    for name in ("qkv", "o", "gate_up", "down"):
+        K, N, lid = awq_inputs.layer(MODEL, name)
+        gen.manual_seed(1000 + lid)
+        qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
+        inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+        ncp = max(4, -(-3 * 126 * 2**20 // gemv_bytes(1, N, K)))
+        copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(ncp - 1)]
+        row = {}
+        for M in BATCHED_M:
+            X = torch.randn((M, K), generator=gen, device=dev).half()
+            Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+            fns = [("gemm", lambda X=X, Y=Y, ws=ws: [awq.gemm(X, q, s_, z, inv_s, out=Y, workspace=ws)
+                                                     for q, s_, z in copies])]
+            if M <= 8:
+                fns.insert(0, ("gemv", lambda X=X, Y=Y: [awq.gemv(X, q, s_, z, inv_s, out=Y)
+                                                         for q, s_, z in copies]))
+            for kind, fn in fns:
+                g = capture(torch, fn)
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(reps):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1000 / (reps * ncp)
+                gbs = gemv_bytes(M, N, K) / us / 1e3
+                tf = 2.0 * M * N * K / us / 1e6
+                row[f"M{M} {kind}"] = {"us": round(us, 2), "GB/s": round(gbs, 1),
+                                       "hbm_frac": round(gbs / hbm, 3), "TFLOP/s": round(tf, 1),
+                                       "tensor_frac": round(tf / peak, 3)}
+                del g
+            del X, Y, ws
+        out[f"{name} {K}->{N}"] = row
+        del copies, qw, sc, zs
+        torch.cuda.empty_cache()
+    return out
+
+
 SWEEP_M = (1, 4, 8, 16, 64, 128, 256, 512, 1024, 2048, 4096)
 
 
@@ -584,6 +637,7 @@ def main():
     ap.add_argument("--no-70b", action="store_true", help="skip the 70B-shape GEMV figures")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused gate/up figures")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 70B token-count sweep")
+    ap.add_argument("--no-batched", action="store_true", help="skip the 7B batched-decode figures")
     ap.add_argument("--no-clip", action="store_true", help="skip the clipping-search timing")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the quantization-variant figures")
@@ -725,6 +779,7 @@ def main():
     fused = None if args.no_fused else fused_gate_up(awq, torch, hbm, pk)
     var = None if args.no_variants else variants(awq, torch, hbm, pk)
     sweep = None if args.no_sweep else sweep_70b(awq, torch, hbm, pk)
+    batched = None if args.no_batched else batched_7b(awq, torch, hbm, pk)
     clip = None if args.no_clip else clip_run(awq, torch)
     search = None if args.no_search else search_run(awq, torch)
     awq.check_device_error()
@@ -764,6 +819,7 @@ def main():
         "fused_gate_up": fused,
         "variants": var,
         "sweep_70b": sweep,
+        "batched_7b": batched,
         "clip": clip,
         "gemm_prefill": gemm,
         "search": search,

@@ -138,6 +138,9 @@ const char* awq_last_error_string(void) { return g_err; }
 int awq_check_device_error(void* stream) {
   unsigned flags = 0;
   AWQ_TRY(read_clear_gemm_error(static_cast<cudaStream_t>(stream), &flags));
+  unsigned narrow = 0;
+  AWQ_TRY(read_clear_narrow_error(static_cast<cudaStream_t>(stream), &narrow));
+  flags |= narrow << 8;
   if (flags) {
     set_error("a tensor-core matmul kernel gave up on a bounded wait (flags 0x%x)", flags);
     return AWQ_ERR_DEVICE;

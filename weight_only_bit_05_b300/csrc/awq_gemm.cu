@@ -595,16 +595,8 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   cfg.numAttrs = 1;
   AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM, BITS>, tb, ta, scales, zeros,
                                   M, N, K, gs, out, ldo, yref, ldy, splits, kps, part));
-  if (splits > 1) {
-    // ldo == N for the split-K plan: the partials and Y are dense [M][N]
-    const int64_t mn4 = static_cast<int64_t>(M) * N / 4;
-    cudaLaunchConfig_t rc = cfg;
-    rc.gridDim = dim3(static_cast<unsigned>(sms * 4), 1, 1);
-    rc.blockDim = dim3(256, 1, 1);
-    rc.dynamicSmemBytes = 0;
-    AWQ_CUDA_TRY(cudaLaunchKernelEx(&rc, splitk_reduce_kernel, static_cast<const float*>(part),
-                                    splits, mn4, static_cast<__half*>(out)));
-  }
+  // ldo == N for the split-K plan: the partials and Y are dense [M][N]
+  if (splits > 1) return launch_splitk_reduce(part, splits, M, N, static_cast<__half*>(out), st);
   return AWQ_OK;
 }
 
@@ -695,7 +687,25 @@ GemmPlan plan_gemm(int M, int N, int K, int mode) {
 
 size_t gemm_partial_bytes(int M, int N, int K) {
   const GemmPlan p = plan_gemm(M, N, K, kGemmOutF16);
-  return p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 0;
+  const size_t wide = p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 0;
+  const size_t narrow = narrow_partial_bytes(M, N, K);
+  return wide > narrow ? wide : narrow;
+}
+
+int launch_splitk_reduce(const float* part, int splits, int M, int N, __half* Y,
+                         cudaStream_t st) {
+  const int64_t mn4 = static_cast<int64_t>(M) * N / 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sm_count() * 4), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, part, splits, mn4, Y));
+  return AWQ_OK;
 }
 
 int gemm_sqerr_slots(int M) { return (M + 255) / 256; }
@@ -768,6 +778,9 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
     set_error("awq_gemm: w_bit = %d, group = %d is not supported", w_bit, group);
     return AWQ_ERR_UNSUPPORTED;
   }
+  if (mode == kGemmOutF16 && narrow_eligible(M, w_bit, group))
+    return launch_gemm_narrow(Xt, xt_permuted, M, qweight, scales, zeros, N, K,
+                              static_cast<__half*>(out), ldo, st, w_bit, group, part, part_bytes);
   GemmPlan plan = plan_gemm(M, N, K, mode);
   // split-K needs the partial sums' workspace and a dense [M][N] output
   if (plan.splits > 1 &&

@@ -73,5 +73,26 @@ GemmPlan plan_gemm(int M, int N, int K, int mode);
 size_t gemm_partial_bytes(int M, int N, int K);   // split-K workspace of the plain matmul
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
+// Y[m][n] = fp16(sum over s < splits of part[s][m][n]), part fp32 [splits][M][N].
+int launch_splitk_reduce(const float* part, int splits, int M, int N, __half* Y,
+                         cudaStream_t st);
+
+// awq_gemm_narrow.cu: the plain fp16-output matmul for M <= 64 tokens, 4- or
+// 8-bit codes in 128- or 64-channel groups (per-group tensor-memory
+// accumulators, steps applied in fp32 by the epilogue).
+struct NarrowPlan {
+  int bn;       // token-tile width (0: not eligible)
+  int splits;   // split-K factor
+  int kps;      // stages per split
+  int bks;      // input channels per stage
+};
+bool narrow_eligible(int M, int w_bit, int group);
+NarrowPlan plan_narrow(int M, int N, int K, int w_bit, int group);
+size_t narrow_partial_bytes(int M, int N, int K);   // split-K workspace, any eligible format
+int launch_gemm_narrow(const __half* Xt, bool xt_permuted, int M, const uint32_t* qweight,
+                       const __half* scales, const uint32_t* zeros, int N, int K, __half* out,
+                       int ldo, cudaStream_t st, int w_bit, int group, float* part,
+                       size_t part_bytes);
+int read_clear_narrow_error(cudaStream_t st, unsigned* flags);
 
 }  // namespace awq
