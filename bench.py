@@ -514,7 +514,8 @@ SWEEP_M = (1, 4, 8, 16, 64, 128, 256, 512, 1024, 2048, 4096)
 
 
 def sweep_70b(awq, torch, hbm, pk, reps=5):
-    """The Llama-2-70B layers over the token count M: awq_gemv for M <= 8,
+    """The Llama-2-70B layers over the token count M: awq_gemv for M = 1,
+    both awq_gemv and awq_gemm for M = 4 and 8 (keys "M4 gemv", "M4 gemm"),
     awq_gemm above; GB/s of the algorithmic bytes and TFLOP/s of 2 M N K."""
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
@@ -526,10 +527,11 @@ def sweep_70b(awq, torch, hbm, pk, reps=5):
         qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
         inv_s = torch.ones(K, dtype=torch.float32, device=dev)
         row = {}
-        for M in SWEEP_M:
+        for M, kind in [(m, k) for m in SWEEP_M
+                        for k in (("gemv",) if m == 1 else ("gemv", "gemm") if m <= 8 else ("gemm",))]:
             X = torch.randn((M, K), generator=gen, device=dev).half()
             Y = torch.empty((M, N), dtype=torch.float16, device=dev)
-            if M <= 8:
+            if kind == "gemv":
                 fn = lambda X=X, Y=Y: awq.gemv(X, qw, sc, zs, inv_s, out=Y)
             else:
                 ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
@@ -547,7 +549,8 @@ def sweep_70b(awq, torch, hbm, pk, reps=5):
             us = e0.elapsed_time(e1) * 1000 / reps
             gbs = gemv_bytes(M, N, K) / us / 1e3
             tf = 2.0 * M * N * K / us / 1e6
-            row[f"M{M}"] = {"us": round(us, 1), "GB/s": round(gbs, 1), "TFLOP/s": round(tf, 1),
+            key = f"M{M} {kind}" if 1 < M <= 8 else f"M{M}"
+            row[key] = {"us": round(us, 1), "GB/s": round(gbs, 1), "TFLOP/s": round(tf, 1),
                             "hbm_frac": round(gbs / hbm, 3), "tensor_frac": round(tf / peak, 3)}
             del g, X, Y
         out[f"{name} {K}->{N}"] = row

@@ -149,7 +149,8 @@ AWQ_API int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
  * reduced inside a thread-block cluster through distributed shared memory.
  * ("awq-quantization" skill page, 主要功能: the GEMV kernel serves batch-1
  * token generation.)  X: fp16 [M][K], 1 <= M <= 8. inv_s: fp32 [K] or NULL
- * (all ones). Y: fp16 [M][N]. */
+ * (all ones). Y: fp16 [M][N]. Its cost grows with M (M fp32 products per
+ * weight); on B300 awq_gemm is the faster call from M = 4 on. */
 AWQ_API int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight,
              const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
              int32_t N, int32_t K, uint16_t* Y, void* stream);
@@ -164,8 +165,13 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
  * Same result as awq_gemv for any M >= 1, on the 5th-generation tensor cores:
  * packed codes and activations staged by TMA, codes dequantized to fp16 in
  * shared memory, tcgen05.mma (fp16 x fp16, fp32 accumulation in tensor
- * memory). ("awq-quantization" skill page, 主要功能: the GEMM kernel serves
- * batch > 1.) When inv_s is not NULL, X~ = fp16(X * inv_s) is first written
+ * memory). For M <= 64 with 4- or 8-bit codes in 128- or 64-channel groups
+ * a narrow-token kernel runs instead: the operand holds the exact integers
+ * q - z in tensor memory, each group's partial sum is accumulated on its own
+ * and multiplied by the group step in fp32 (so it rounds differently from
+ * the wide kernel, within the same bound). ("awq-quantization" skill page,
+ * 主要功能: the GEMM kernel serves batch > 1.) When inv_s is not NULL,
+ * X~ = fp16(X * inv_s) is first written
  * to the workspace; with inv_s == NULL X is read directly and the workspace
  * may be NULL. awq_gemm_workspace_size also counts the fp32 partial sums of a
  * split-K launch (chosen when the layer has too few 128-row tiles to fill the

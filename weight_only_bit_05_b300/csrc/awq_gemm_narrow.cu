@@ -14,9 +14,10 @@
 //    i), which removes the 4x-expanded fp16 tile's write and read from the
 //    shared-memory bandwidth; shared memory only holds the packed codes and
 //    the activation tile, in a deep ring (16..24 stages) released by the MMA;
-//  * two teams of four dequantization warps take alternate stages, each
-//    thread one whole weight row of its stage (16 or 8 chunks of 8 codes),
-//    written with tcgen05.st into a ring of 4..8 operand stages;
+//  * three teams (two at 64 tokens) of four dequantization warps take the
+//    stages in turn, each thread one whole weight row of its stage (16 or 8
+//    chunks of 8 codes), written with tcgen05.st into a ring of 4..8
+//    operand stages;
 //  * the operand holds the exact integers q - z (HSUB2 of fp16 magic
 //    numbers, no rounding), and each group's partial product accumulates in
 //    its own tensor-memory accumulator (a ring of four); the epilogue warps
@@ -32,11 +33,11 @@
 //
 // Warp roles: warp 0 issues TMA (codes [128 rows x 16 words], activations
 // [BN x 64] per 64 channels, 128-byte swizzle); warp 1 allocates tensor
-// memory and issues tcgen05.mma (one thread); warps 2..9 dequantize;
-// warps 10..13 run the per-group epilogue.  Every mbarrier wait is bounded
-// (1 s); on expiry the kernel records the fact in a device word, makes the
-// other roles stop, drains its copies and MMAs, frees tensor memory and
-// returns.
+// memory and issues tcgen05.mma (one thread); the next 12 (8) warps
+// dequantize; the last 4 run the per-group epilogue.  Every mbarrier wait
+// is bounded (1 s); on expiry the kernel records the fact in a device word,
+// makes the other roles stop, drains its copies and MMAs, frees tensor
+// memory and returns.
 #include "awq_internal.h"
 
 namespace awq {
@@ -46,16 +47,18 @@ __device__ unsigned int g_narrow_error = 0;
 namespace {
 
 constexpr int NBM = 128;                  // weight rows per tile (MMA M)
-constexpr int kTeams = 2;                 // dequantization teams of 4 warps
-constexpr int kNDeqWarps = 4 * kTeams;
 constexpr int kNEpiWarps = 4;
-constexpr int kNThreads = 32 * (2 + kNDeqWarps + kNEpiWarps);
 constexpr int kNRing = 4;                 // group accumulators in flight
 constexpr uint64_t kNWaitNs = 1000000000ull;
 constexpr int kNSmemBudget = 227 * 1024;
 
 template <int BN, int BITS, int BKS>
 struct NCfg {
+  // dequantization teams of 4 warps: three while the epilogue's output row
+  // (BN registers) is short, two at BN = 64 to stay clear of spills
+  static constexpr int TEAMS = BN <= 32 ? 3 : 2;
+  static constexpr int DEQ_WARPS = 4 * TEAMS;
+  static constexpr int THREADS = 32 * (2 + DEQ_WARPS + kNEpiWarps);
   static constexpr int NATOM = BKS / 64;                // 128-byte swizzle atoms per row
   static constexpr int RAW_ROW = BKS * BITS / 8;        // packed bytes of a row per stage
   static constexpr int RAW_BYTES = NBM * RAW_ROW;
@@ -170,7 +173,7 @@ __device__ __forceinline__ uint4 codes8_minus_zero(uint32_t w0, uint32_t w1, uin
 // stages of BKS channels each, a whole number of groups).  gs_shift =
 // log2(group), spg_shift = log2(group / BKS).
 template <int BN, bool PERM, int BITS, int BKS>
-__global__ void __launch_bounds__(kNThreads, 1)
+__global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
     gemm_narrow_kernel(const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_q,
                        const __half* __restrict__ scales, const uint32_t* __restrict__ zeros,
@@ -281,7 +284,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // the whole warp walks the stages; one elected lane issues the MMAs
+    // The whole warp walks the stages; one elected lane issues the MMAs.
+    // Any shared-memory access of this warp, an mbarrier wait included,
+    // waits until the MMAs it has queued drain (~160 cycles, measured), so
+    // it waits on one barrier per stage: a_full, which the dequantization
+    // team arrives on only after it has seen the stage's codes and
+    // activations land (raw_full) and, at a group's first stage, the
+    // group's accumulator freed by the epilogue (g_empty).
     constexpr uint32_t idesc = idesc_f16_f32(NBM, BN);
     int it = 0, gcount = 0, slot = 0;
     bool ok = true;
@@ -292,10 +301,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
         const int rs = it % SR, as = it % SA;
         const bool first = (kb & spg_mask) == 0;
         if (first) slot = gcount % kNRing;
-        bool got = nwait(a_full + as, (it / SA) & 1, ab, 2u) &&
-                   nwait(raw_full + rs, (it / SR) & 1, ab, 2u);
-        if (got && first && gcount >= kNRing)
-          got = nwait(g_empty + slot, ((gcount / kNRing) - 1) & 1, ab, 2u);
+        const bool got = nwait(a_full + as, (it / SA) & 1, ab, 2u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
         break;
       }
     __syncwarp();
-  } else if (warp < 2 + kNDeqWarps) {
+  } else if (warp < 2 + C::DEQ_WARPS) {
     // ------------------------------------------------------------ dequant
     const int dw = warp - 2;
     const int team = dw >> 2;
@@ -349,7 +355,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
       int kb0, kb1;
       krange(t, kb0, kb1);
       const int it0 = it;
-      // this team's first stage of the item: (it0 + kb - kb0) % kTeams == team
+      // this team's first stage of the item: (it0 + kb - kb0) % TEAMS == team
+      constexpr int kTeams = C::TEAMS;
       int kb = kb0 + ((team - it0) % kTeams + kTeams) % kTeams;
       int zwi = ((kb * BKS) >> gs_shift) >> PW_SHIFT;
       uint32_t zcur = zload(zwi), znext = zload(zwi + 1);
@@ -368,6 +375,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
         const int rs = sit % SR, as = sit % SA;
         bool got = nwait(raw_full + rs, (sit / SR) & 1, ab, 4u);
         if (got && sit >= SA) got = nwait(a_empty + as, ((sit / SA) - 1) & 1, ab, 4u);
+        // the first stage of a group also waits until the epilogue has freed
+        // the group's accumulator, so that the MMA warp waits on a_full alone
+        // (groups never straddle items, so the CTA's group ordinal is
+        // sit >> spg_shift)
+        const int gidx = sit >> spg_shift;
+        if (got && (kb & spg_mask) == 0 && gidx >= kNRing)
+          got = nwait(g_empty + gidx % kNRing, ((gidx / kNRing) - 1) & 1, ab, 4u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -505,7 +519,7 @@ int launch_narrow_tile(const CUtensorMap& tx, const CUtensorMap& tq, const __hal
   const int items = ((N + NBM - 1) / NBM) * ((M + BN - 1) / BN) * splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(items < sms ? items : sms, 1, 1);
-  cfg.blockDim = dim3(kNThreads, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
