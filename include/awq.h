@@ -165,7 +165,7 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
  * Same result as awq_gemv for any M >= 1, on the 5th-generation tensor cores:
  * packed codes and activations staged by TMA, codes dequantized to fp16 in
  * shared memory, tcgen05.mma (fp16 x fp16, fp32 accumulation in tensor
- * memory). For M <= 64 with 4- or 8-bit codes in 128- or 64-channel groups
+ * memory). For M <= 128 with 4- or 8-bit codes in 128- or 64-channel groups
  * a narrow-token kernel runs instead: the operand holds the exact integers
  * q - z in tensor memory, each group's partial sum is accumulated on its own
  * and multiplied by the group step in fp32 (so it rounds differently from

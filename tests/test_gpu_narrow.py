@@ -1,11 +1,11 @@
-"""GPU parity of the narrow-token tensor-core matmul (M <= 64 tokens, plain
+"""GPU parity of the narrow-token tensor-core matmul (M <= 128 tokens, plain
 fp16 output, 4- or 8-bit codes in 128- or 64-channel groups).
 
 Its weights enter the MMA as the exact integers q - z and every group's
 partial product is scaled by s in fp32, so it rounds differently from the
 wide-tile kernel; the bound is the same per-element one against the oracle:
 |y_gpu - y_ref| <= 4e-3 sum_k |x~ w^| + 1 fp16 ulp.  Cases cover every token
-tile (16, 32, 64 and ragged M), both activation layouts (prescaled and
+tile (16, 32, 64, 128 and ragged M), both activation layouts (prescaled and
 k-permuted, or the caller's in natural order), ragged N, long K (many
 zero-point words per row), split-K against the unsplit launch, several work
 items per CTA, and the Llama-2-7B batched-decode shapes on sampled outputs.
@@ -52,7 +52,7 @@ def _gemm(X16, qw, sc, zs, inv_s, w_bit, group, zp, workspace=None):
 
 
 @pytest.mark.parametrize("w_bit,group,zp", FORMATS, ids=FIDS)
-@pytest.mark.parametrize("M", [1, 8, 16, 17, 32, 48, 64])
+@pytest.mark.parametrize("M", [1, 8, 16, 17, 32, 48, 64, 65, 100, 128])
 @pytest.mark.parametrize("scaled", [True, False])
 def test_narrow_matches_oracle(w_bit, group, zp, M, scaled):
     # N = 3 full 128-row tiles + 8 rows; K = 12 groups of 128 (24 of 64)
@@ -76,7 +76,8 @@ def test_narrow_long_k_and_outliers(w_bit, group):
            w_bit)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 256, 4096), (40, 512, 8192), (8, 384, 11008)])
+@pytest.mark.parametrize("M,N,K", [(16, 256, 4096), (40, 512, 8192), (8, 384, 11008),
+                                   (120, 256, 4096)])
 def test_narrow_splitk_matches_unsplit(M, N, K):
     # these shapes have few tiles, so the plan splits K when the workspace
     # holds the partial sums; without it the launch runs unsplit
@@ -105,7 +106,7 @@ def test_narrow_many_items_per_cta():
 
 
 @pytest.mark.parametrize("layer", ["qkv", "o", "gate_up", "down"])
-@pytest.mark.parametrize("M", [8, 32])
+@pytest.mark.parametrize("M", [8, 32, 128])
 def test_narrow_7b_batched_sampled(layer, M):
     # Llama-2-7B layer shapes at batched decode, on sampled output channels
     K, N, lid = awq_inputs.layer("llama2-7b", layer)

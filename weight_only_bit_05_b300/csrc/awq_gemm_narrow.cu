@@ -1,4 +1,4 @@
-// W4A16 matmul for few tokens (M <= 64) on the 5th-generation tensor cores.
+// W4A16 matmul for few tokens (M <= 128) on the 5th-generation tensor cores.
 //
 // "awq-quantization（AWQ量化技术）Skill" page, section 主要功能和特点: the GEMM
 // kernel serves batch > 1.  With a handful of tokens the layer reads every
@@ -14,7 +14,7 @@
 //    i), which removes the 4x-expanded fp16 tile's write and read from the
 //    shared-memory bandwidth; shared memory only holds the packed codes and
 //    the activation tile, in a deep ring (16..24 stages) released by the MMA;
-//  * three teams (two at 64 tokens) of four dequantization warps take the
+//  * three teams (two at 64 and 128 tokens) of four dequantization warps take the
 //    stages in turn, each thread one whole weight row of its stage (16 or 8
 //    chunks of 8 codes), written with tcgen05.st into a ring of 4..8
 //    operand stages;
@@ -34,7 +34,7 @@
 // Warp roles: warp 0 issues TMA (codes [128 rows x 16 words], activations
 // [BN x 64] per 64 channels, 128-byte swizzle); warp 1 allocates tensor
 // memory and issues tcgen05.mma (one thread); the next 12 (8) warps
-// dequantize; the last 4 run the per-group epilogue.  Every mbarrier wait
+// dequantize; the last 4 (8 at 128 tokens) run the per-group epilogue.  Every mbarrier wait
 // is bounded (1 s); on expiry the kernel records the fact in a device word,
 // makes the other roles stop, drains its copies and MMAs, frees tensor
 // memory and returns.
@@ -47,8 +47,6 @@ __device__ unsigned int g_narrow_error = 0;
 namespace {
 
 constexpr int NBM = 128;                  // weight rows per tile (MMA M)
-constexpr int kNEpiWarps = 4;
-constexpr int kNRing = 4;                 // group accumulators in flight
 constexpr uint64_t kNWaitNs = 1000000000ull;
 constexpr int kNSmemBudget = 227 * 1024;
 
@@ -58,7 +56,11 @@ struct NCfg {
   // (BN registers) is short, two at BN = 64 to stay clear of spills
   static constexpr int TEAMS = BN <= 32 ? 3 : 2;
   static constexpr int DEQ_WARPS = 4 * TEAMS;
-  static constexpr int THREADS = 32 * (2 + DEQ_WARPS + kNEpiWarps);
+  // epilogue: 4 warps (one per tensor-memory lane quarter), 8 at BN = 128,
+  // each pair of a quarter taking half of the token columns
+  static constexpr int EPI_WARPS = BN == 128 ? 8 : 4;
+  static constexpr int EPI_COLS = BN * 4 / EPI_WARPS;
+  static constexpr int THREADS = 32 * (2 + DEQ_WARPS + EPI_WARPS);
   static constexpr int NATOM = BKS / 64;                // 128-byte swizzle atoms per row
   static constexpr int RAW_ROW = BKS * BITS / 8;        // packed bytes of a row per stage
   static constexpr int RAW_BYTES = NBM * RAW_ROW;
@@ -67,10 +69,12 @@ struct NCfg {
   static constexpr int CTRL = 1024;                     // barriers, tmem slot, flag
   static constexpr int SR_FIT = (kNSmemBudget - 1024 - CTRL) / RSLOT;
   static constexpr int SR = SR_FIT > 24 ? 24 : SR_FIT;
-  // tensor memory (512 columns): kNRing group accumulators, then the operand
-  // ring, BKS / 2 columns (two fp16 per column) per stage
+  // tensor memory (512 columns): NRING group accumulators (groups in flight
+  // between the MMA and the epilogue), then the operand ring, BKS / 2
+  // columns (two fp16 per column) per stage
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;
-  static constexpr int A_COL0 = kNRing * ACC_COLS;
+  static constexpr int NRING = BN == 128 ? 2 : 4;
+  static constexpr int A_COL0 = NRING * ACC_COLS;
   static constexpr int A_COLS = BKS / 2;
   static constexpr int SA_FIT = (512 - A_COL0) / A_COLS;
   static constexpr int SA = SA_FIT > 8 ? 8 : SA_FIT;
@@ -196,8 +200,8 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
   uint64_t* a_full = raw_empty + SR;
   uint64_t* a_empty = a_full + SA;
   uint64_t* g_full = a_empty + SA;
-  uint64_t* g_empty = g_full + kNRing;
-  uint64_t* drain = g_empty + kNRing;
+  uint64_t* g_empty = g_full + C::NRING;
+  uint64_t* drain = g_empty + C::NRING;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const NAbort ab{abort_flag};
@@ -221,9 +225,9 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
       mbar_init(a_full + s, 4);                     // one arrival per warp of a team
       mbar_init(a_empty + s, 1);
     }
-    for (int b = 0; b < kNRing; ++b) {
+    for (int b = 0; b < C::NRING; ++b) {
       mbar_init(g_full + b, 1);
-      mbar_init(g_empty + b, 32 * kNEpiWarps);
+      mbar_init(g_empty + b, 32 * C::EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const int rs = it % SR, as = it % SA;
         const bool first = (kb & spg_mask) == 0;
-        if (first) slot = gcount % kNRing;
+        if (first) slot = gcount % C::NRING;
         const bool got = nwait(a_full + as, (it / SA) & 1, ab, 2u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
@@ -380,8 +384,8 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
         // (groups never straddle items, so the CTA's group ordinal is
         // sit >> spg_shift)
         const int gidx = sit >> spg_shift;
-        if (got && (kb & spg_mask) == 0 && gidx >= kNRing)
-          got = nwait(g_empty + gidx % kNRing, ((gidx / kNRing) - 1) & 1, ab, 4u);
+        if (got && (kb & spg_mask) == 0 && gidx >= C::NRING)
+          got = nwait(g_empty + gidx % C::NRING, ((gidx / C::NRING) - 1) & 1, ab, 4u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -423,6 +427,8 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;                  // tensor-memory lanes 32q .. 32q + 31
+    constexpr int EC = C::EPI_COLS;
+    const int cb = ((warp - 2 - C::DEQ_WARPS) >> 2) * EC;   // first token column
     const int G = K >> gs_shift;
     int gcount = 0;
     for (int t = blockIdx.x; t < items; t += gridDim.x) {
@@ -439,13 +445,13 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
 #pragma unroll
       for (int i = 0; i < AHEAD; ++i)
         sq[i] = (row_ok && g0 + i < g1) ? __half2float(srow[g0 + i]) : 0.f;
-      float y[BN];
+      float y[EC];
 #pragma unroll
-      for (int j = 0; j < BN; ++j) y[j] = 0.f;
+      for (int j = 0; j < EC; ++j) y[j] = 0.f;
       bool ok = true;
       for (int g = g0; g < g1; ++g, ++gcount) {
-        const int slot = gcount % kNRing;
-        const bool got = nwait(g_full + slot, (gcount / kNRing) & 1, ab, 8u);
+        const int slot = gcount % C::NRING;
+        const bool got = nwait(g_full + slot, (gcount / C::NRING) & 1, ab, 8u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -456,9 +462,9 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
         for (int i = 0; i + 1 < AHEAD; ++i) sq[i] = sq[i + 1];
         sq[AHEAD - 1] = (row_ok && g + AHEAD < g1) ? __half2float(srow[g + AHEAD]) : 0.f;
         const uint32_t gaddr =
-            tmem + slot * C::ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16);
+            tmem + slot * C::ACC_COLS + cb + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = 0; c0 < EC; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(gaddr + c0, v);
           tmem_ld_wait();
@@ -471,8 +477,8 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
       if (!ok) break;
       float* pout = part + static_cast<size_t>(t % splits) * M * ldo;   // splits > 1
 #pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        const int m = m0 + j;
+      for (int j = 0; j < EC; ++j) {
+        const int m = m0 + cb + j;
         if (m < M && row_ok) {
           const size_t idx = static_cast<size_t>(m) * ldo + n;
           if (splits > 1)
@@ -545,9 +551,12 @@ int dispatch_narrow(int bn, const CUtensorMap& tx, const CUtensorMap& tq, const 
     case 32:
       return launch_narrow_tile<32, PERM, BITS, BKS>(tx, tq, scales, zeros, M, N, K, gs_shift,
                                                      spg_shift, out, ldo, splits, kps, part, st);
-    default:
+    case 64:
       return launch_narrow_tile<64, PERM, BITS, BKS>(tx, tq, scales, zeros, M, N, K, gs_shift,
                                                      spg_shift, out, ldo, splits, kps, part, st);
+    default:
+      return launch_narrow_tile<128, PERM, BITS, BKS>(tx, tq, scales, zeros, M, N, K, gs_shift,
+                                                      spg_shift, out, ldo, splits, kps, part, st);
   }
 }
 
@@ -556,7 +565,8 @@ int stage_channels(int w_bit, int group) { return (w_bit == 4 && group == 128) ?
 }  // namespace
 
 bool narrow_eligible(int M, int w_bit, int group) {
-  return M >= 1 && M <= 64 && (w_bit == 4 || w_bit == 8) && (group == 128 || group == 64);
+  return M >= 1 && M <= kNarrowMaxM && (w_bit == 4 || w_bit == 8) &&
+         (group == 128 || group == 64);
 }
 
 // Token tile and split-K, from a cost model in SM cycles fitted to B300
@@ -573,7 +583,7 @@ NarrowPlan plan_narrow(int M, int N, int K, int w_bit, int group) {
   const int bks = stage_channels(w_bit, group);
   const int spg = group / bks;
   const int nk = K / bks;
-  const int bn = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+  const int bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   const int sms = sms_here();
   const int tiles = ((N + NBM - 1) / NBM) * ((M + bn - 1) / bn);
   const double stage_cycles =

@@ -77,9 +77,10 @@ int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
 int launch_splitk_reduce(const float* part, int splits, int M, int N, __half* Y,
                          cudaStream_t st);
 
-// awq_gemm_narrow.cu: the plain fp16-output matmul for M <= 64 tokens, 4- or
+// awq_gemm_narrow.cu: the plain fp16-output matmul for M <= 128 tokens, 4- or
 // 8-bit codes in 128- or 64-channel groups (per-group tensor-memory
 // accumulators, steps applied in fp32 by the epilogue).
+constexpr int kNarrowMaxM = 128;
 struct NarrowPlan {
   int bn;       // token-tile width (0: not eligible)
   int splits;   // split-K factor
