@@ -510,12 +510,12 @@ def batched_7b(awq, torch, hbm, pk, reps=10):
     return out
 
 
-SWEEP_M = (1, 4, 8, 16, 64, 128, 256, 512, 1024, 2048, 4096)
+SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
 
 
 def sweep_70b(awq, torch, hbm, pk, reps=5):
     """The Llama-2-70B layers over the token count M: awq_gemv for M = 1,
-    both awq_gemv and awq_gemm for M = 4 and 8 (keys "M4 gemv", "M4 gemm"),
+    both awq_gemv and awq_gemm for M = 2, 4 and 8 (keys "M4 gemv", "M4 gemm"),
     awq_gemm above; GB/s of the algorithmic bytes and TFLOP/s of 2 M N K."""
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
@@ -587,6 +587,49 @@ def clip_run(awq, torch, model=MODEL, name="qkv", T=4096, n_clip=20):
             "includes": "group Gram matrices, n_clip quadratic forms per group, argmin"}
 
 
+def toy_512(awq, torch, reps=100):
+    """The single 512 -> 512 linear: the AWQ quantizer on 256 calibration
+    tokens (statistics, 20-alpha search, pack of the chosen scales) and the
+    quantized layer at M = 1 (awq_gemv) and M = 16 (awq_gemm); times only (the
+    layer is 0.14 MB, latency-bound)."""
+    dev = torch.device("cuda")
+    K, N, lid = awq_inputs.layer("toy", "linear")
+    W = torch.from_numpy(awq_inputs.weight(N, K, lid)).to(dev)
+    Xc = torch.from_numpy(awq_inputs.calib_tokens(256, K, lid)).to(dev)
+    awq.search(Xc, W)   # warm-up (kernel attributes)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    res = awq.search(Xc, W)
+    qw, sc, zs = awq.pack(W, res["s_c"])
+    torch.cuda.synchronize()
+    t_quant = time.perf_counter() - t0
+    out = {"layer": f"toy {K}->{N}", "calib_tokens": 256, "alpha": res["alpha"],
+           "quantize_ms": round(1000 * t_quant, 3),
+           "quantize_includes": "statistics, 20-alpha search, pack (host argmin and launches)"}
+    for M, kind in ((1, "gemv"), (16, "gemm")):
+        X = torch.from_numpy(awq_inputs.timed_tokens(M, K, lid)).to(dev)
+        Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        inv = res["inv_s"]
+        if kind == "gemv":
+            fn = lambda X=X, Y=Y: [awq.gemv(X, qw, sc, zs, inv, out=Y) for _ in range(reps)]
+        else:
+            ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+            fn = lambda X=X, Y=Y, ws=ws: [awq.gemm(X, qw, sc, zs, inv, out=Y, workspace=ws)
+                                          for _ in range(reps)]
+        g = capture(torch, fn)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[f"M{M} {kind} us"] = round(e0.elapsed_time(e1) * 1000 / reps, 2)
+        del g
+    return out
+
+
 def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
     """Wall time of awq_search_scales on one layer (20 alphas) and the
     TFLOP/s of its tensor-core work (Y_ref once + 20 squared-error passes)."""
@@ -642,6 +685,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the 70B token-count sweep")
     ap.add_argument("--no-batched", action="store_true", help="skip the 7B batched-decode figures")
     ap.add_argument("--no-clip", action="store_true", help="skip the clipping-search timing")
+    ap.add_argument("--no-toy", action="store_true", help="skip the 512 -> 512 toy layer")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the quantization-variant figures")
     ap.add_argument("--only-gemm", default=None, metavar="MODEL:LAYER:M",
@@ -784,6 +828,7 @@ def main():
     sweep = None if args.no_sweep else sweep_70b(awq, torch, hbm, pk)
     batched = None if args.no_batched else batched_7b(awq, torch, hbm, pk)
     clip = None if args.no_clip else clip_run(awq, torch)
+    toy = None if args.no_toy else toy_512(awq, torch)
     search = None if args.no_search else search_run(awq, torch)
     awq.check_device_error()
 
@@ -824,6 +869,7 @@ def main():
         "sweep_70b": sweep,
         "batched_7b": batched,
         "clip": clip,
+        "toy_512": toy,
         "gemm_prefill": gemm,
         "search": search,
     }
