@@ -32,6 +32,12 @@ def test_default_config_and_workspace_sizes():
     c = lib.awq_default_config()
     assert (c.w_bit, c.group, c.zero_point, c.n_grid) == (4, 128, 1, 20)
     assert lib.awq_gemm_workspace_size(16, 512, 512) == 16 * 512 * 2
+    # few 128-row tiles: the plans split K, and the workspace also holds the
+    # fp32 partial sums (narrow-token kernel up to 128 tokens, wide above)
+    for M, N, K in ((16, 256, 4096), (120, 256, 4096), (48, 640, 8192), (300, 1024, 8192)):
+        xt = ((M * K * 2 + 255) // 256) * 256
+        part = lib.awq_gemm_workspace_size(M, N, K) - xt
+        assert part > 0 and part % (M * N * 4) == 0 and part // (M * N * 4) <= 8, (M, N, K)
     assert lib.awq_gemm_workspace_size(0, 512, 512) == 0
     assert lib.awq_absmean_workspace_size(4096, 4096) % 8 == 0
     assert lib.awq_absmean_workspace_size(4096, 4096) >= 4096 * 8

@@ -632,6 +632,8 @@ int pick_bn(int M, int mode) {
   return 256;
 }
 
+}  // namespace
+
 int sm_count() {
   static int sms = 0;
   if (!sms) {
@@ -642,8 +644,6 @@ int sm_count() {
   }
   return sms;
 }
-
-}  // namespace
 
 // Token-tile width and split-K for one launch.  The tile is the smallest of
 // 16..256 tokens that holds M; split-K comes from a cost model in SM cycles:

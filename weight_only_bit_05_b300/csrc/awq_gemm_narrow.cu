@@ -498,17 +498,6 @@ __global__ void __launch_bounds__(NCfg<BN, BITS, BKS>::THREADS, 1)
   }
 }
 
-int sms_here() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 148;
-  }
-  return sms;
-}
-
 template <int BN, bool PERM, int BITS, int BKS>
 int launch_narrow_tile(const CUtensorMap& tx, const CUtensorMap& tq, const __half* scales,
                        const uint32_t* zeros, int M, int N, int K, int gs_shift, int spg_shift,
@@ -521,7 +510,7 @@ int launch_narrow_tile(const CUtensorMap& tx, const CUtensorMap& tq, const __hal
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr_set = true;
   }
-  const int sms = sms_here();
+  const int sms = sm_count();
   const int items = ((N + NBM - 1) / NBM) * ((M + BN - 1) / BN) * splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(items < sms ? items : sms, 1, 1);
@@ -584,7 +573,7 @@ NarrowPlan plan_narrow(int M, int N, int K, int w_bit, int group) {
   const int spg = group / bks;
   const int nk = K / bks;
   const int bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-  const int sms = sms_here();
+  const int sms = sm_count();
   const int tiles = ((N + NBM - 1) / NBM) * ((M + bn - 1) / bn);
   const double stage_cycles =
       1000.0 * (1.0 + M / 500.0) * (128.0 * bks * w_bit / 8.0) / 8192.0;

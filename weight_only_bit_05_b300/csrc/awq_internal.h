@@ -73,6 +73,7 @@ GemmPlan plan_gemm(int M, int N, int K, int mode);
 size_t gemm_partial_bytes(int M, int N, int K);   // split-K workspace of the plain matmul
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
+int sm_count();   // SMs of the current device (148 when it cannot be queried)
 // Y[m][n] = fp16(sum over s < splits of part[s][m][n]), part fp32 [splits][M][N].
 int launch_splitk_reduce(const float* part, int splits, int M, int N, __half* Y,
                          cudaStream_t st);
