@@ -14,16 +14,17 @@
 //    i), which removes the 4x-expanded fp16 tile's write and read from the
 //    shared-memory bandwidth; shared memory only holds the packed codes and
 //    the activation tile, in a deep ring (16..24 stages) released by the MMA;
-//  * three teams (two at 64 and 128 tokens) of four dequantization warps take the
-//    stages in turn, each thread one whole weight row of its stage (16 or 8
-//    chunks of 8 codes), written with tcgen05.st into a ring of 4..8
-//    operand stages;
+//  * three teams (two at 64 and 128 tokens) of four dequantization warps
+//    take the stages in turn, each thread one whole weight row of its stage
+//    (16 or 8 chunks of 8 codes), written with tcgen05.st into a ring of
+//    4..8 operand stages;
 //  * the operand holds the exact integers q - z (HSUB2 of fp16 magic
 //    numbers, no rounding), and each group's partial product accumulates in
-//    its own tensor-memory accumulator (a ring of four); the epilogue warps
-//    read it, multiply by the group's step s in fp32 and add it to the
-//    output row they keep in registers.  That takes the multiply by s off
-//    the per-weight path and leaves only the final fp32 sum to round.
+//    its own tensor-memory accumulator (a ring of four, two at 128 tokens);
+//    the epilogue warps read it, multiply by the group's step s in fp32 and
+//    add it to the output row they keep in registers.  That takes the
+//    multiply by s off the per-weight path and leaves only the final fp32
+//    sum to round.
 //
 // A 128 x BN x 16 MMA costs about as much for BN = 16 as for BN = 64 (a
 // fixed ~57 cycles plus ~0.4 cycle per token column, measured on B300), so
@@ -34,10 +35,10 @@
 // Warp roles: warp 0 issues TMA (codes [128 rows x 16 words], activations
 // [BN x 64] per 64 channels, 128-byte swizzle); warp 1 allocates tensor
 // memory and issues tcgen05.mma (one thread); the next 12 (8) warps
-// dequantize; the last 4 (8 at 128 tokens) run the per-group epilogue.  Every mbarrier wait
-// is bounded (1 s); on expiry the kernel records the fact in a device word,
-// makes the other roles stop, drains its copies and MMAs, frees tensor
-// memory and returns.
+// dequantize; the last 4 (8 at 128 tokens) run the per-group epilogue.
+// Every mbarrier wait is bounded (1 s); on expiry the kernel records the fact
+// in a device word, makes the other roles stop, drains its copies and MMAs,
+// frees tensor memory and returns.
 #include "awq_internal.h"
 
 namespace awq {
