@@ -144,13 +144,24 @@ AWQ_API int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
 
 /* ------------------------------------------------------------ GEMV, M <= 8
  * Y[m][n] = fp16( sum_k (X[m][k] * inv_s[k]) * (q[n][k] - z[n][g(k)]) * s[n][g(k)] )
- * on CUDA cores: 128-bit loads of the packed codes, dequantization in
- * registers, fp32 products and sums, warp-shuffle reductions; split-K is
- * reduced inside a thread-block cluster through distributed shared memory.
  * ("awq-quantization" skill page, 主要功能: the GEMV kernel serves batch-1
- * token generation.)  X: fp16 [M][K], 1 <= M <= 8. inv_s: fp32 [K] or NULL
- * (all ones). Y: fp16 [M][N]. Its cost grows with M (M fp32 products per
- * weight); on B300 awq_gemm is the faster call from M = 4 on. */
+ * token generation; "AWQ量化实战" §3.4: decoding is bound by reading the
+ * weights.)  X: fp16 [M][K], 1 <= M <= 8. inv_s: fp32 [K] or NULL (all
+ * ones). Y: fp16 [M][N]. The result is deterministic.
+ * The default format (4-bit codes, 128-channel groups) with K % 256 == 0
+ * streams the packed codes, steps and zero points through TMA and cp.async
+ * into shared memory and reduces on the warp-level tensor-core MMA (exact
+ * products x~ (q - z), fp32 sums, each group's sum times its step in fp32);
+ * other formats and K run on CUDA cores (fp32 products and sums,
+ * warp-shuffle reductions). K is split over a thread-block cluster when the
+ * activations do not fit in shared memory.
+ * Launched with programmatic dependent launch: qweight, scales and zeros are
+ * read BEFORE the kernel waits for the previous kernel on the stream, so that
+ * the weights of consecutive layers stream without a gap. They must therefore
+ * not be written by the kernel launched immediately before this call on the
+ * same stream (awq_pack and awq_pack_clipped end with an empty kernel for
+ * this reason, so calling awq_gemv right after them is safe). X, inv_s and Y
+ * are touched only after the wait. */
 AWQ_API int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight,
              const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
              int32_t N, int32_t K, uint16_t* Y, void* stream);

@@ -146,16 +146,27 @@ def _cfg(w_bit=4, group=128, zero_point=True, n_grid=20):
 
 
 def pack(W: torch.Tensor, s_c: torch.Tensor | None = None, w_bit: int = 4, group: int = 128,
-         zero_point: bool = True):
+         zero_point: bool = True, out=None):
+    """(qweight, scales, zeros) of W; ``out`` = existing (qweight, scales, zeros)
+    buffers to write into."""
     _dev(W, torch.float16, "W")
     if s_c is not None:
         _dev(s_c, torch.float32, "s_c")
     N, K = W.shape
     c = 32 // w_bit
     G = K // group
-    qweight = torch.empty((N, K // c), dtype=torch.int32, device=W.device)
-    scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
-    zeros = torch.empty((N, (G + c - 1) // c), dtype=torch.int32, device=W.device)
+    if out is not None:
+        qweight, scales, zeros = out
+        _dev(qweight, torch.int32, "qweight")
+        _dev(scales, torch.float16, "scales")
+        _dev(zeros, torch.int32, "zeros")
+        if (tuple(qweight.shape), tuple(scales.shape), tuple(zeros.shape)) != \
+                ((N, K // c), (N, G), (N, (G + c - 1) // c)):
+            raise ValueError("pack: out buffers have the wrong shapes")
+    else:
+        qweight = torch.empty((N, K // c), dtype=torch.int32, device=W.device)
+        scales = torch.empty((N, G), dtype=torch.float16, device=W.device)
+        zeros = torch.empty((N, (G + c - 1) // c), dtype=torch.int32, device=W.device)
     cfg = _cfg(w_bit, group, zero_point)
     _check(lib.awq_pack(_ptr(W), _ptr(s_c), N, K, ctypes.byref(cfg), _ptr(qweight), _ptr(scales),
                         _ptr(zeros), _stream()))

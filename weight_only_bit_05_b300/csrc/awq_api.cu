@@ -1,7 +1,11 @@
 // C-ABI entry points: argument validation, status codes and error strings.
 // Every step of the computation runs in the kernels of the other files.
+#include <atomic>
 #include <cstdarg>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "awq_internal.h"
 
@@ -22,6 +26,39 @@ int cuda_status(cudaError_t e, const char* what) {
   return AWQ_ERR_CUDA;
 }
 
+// ------------------------------------------------ per-device launch helpers
+// A process may drive several devices from several host threads: the SM
+// count is cached per device ordinal, and the dynamic shared-memory limit of
+// a kernel is raised once per (kernel, device) under a lock.
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::mutex g_attr_mu;
+std::map<std::pair<const void*, int>, int> g_attr_bytes;
+}  // namespace
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  g_sms[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int ensure_smem_attr(const void* func, int bytes) {
+  int dev = 0;
+  AWQ_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  int& have = g_attr_bytes[std::make_pair(func, dev)];
+  if (have >= bytes) return AWQ_OK;
+  AWQ_CUDA_TRY(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  have = bytes;
+  return AWQ_OK;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -29,16 +66,15 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 static EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+  });
   return fn;
 }
 
@@ -141,6 +177,9 @@ int awq_check_device_error(void* stream) {
   unsigned narrow = 0;
   AWQ_TRY(read_clear_narrow_error(static_cast<cudaStream_t>(stream), &narrow));
   flags |= narrow << 8;
+  unsigned gemv = 0;
+  AWQ_TRY(read_clear_gemv_error(static_cast<cudaStream_t>(stream), &gemv));
+  flags |= gemv << 16;
   if (flags) {
     set_error("a tensor-core matmul kernel gave up on a bounded wait (flags 0x%x)", flags);
     return AWQ_ERR_DEVICE;
@@ -197,9 +236,10 @@ int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K, const aw
   AWQ_TRY(check_ptr(scales, "scales"));
   AWQ_TRY(check_ptr(zeros, "zeros"));
   const awq_config c = cfg ? *cfg : awq_default_config();
-  return launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
-                     reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream),
-                     c.w_bit, c.group, c.zero_point != 0);
+  AWQ_TRY(launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
+                      reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream),
+                      c.w_bit, c.group, c.zero_point != 0));
+  return launch_stream_fence(static_cast<cudaStream_t>(stream));
 }
 
 int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M, const uint32_t* qweight,
@@ -330,9 +370,10 @@ int awq_pack_clipped(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
   AWQ_TRY(check_ptr(scales, "scales"));
   AWQ_TRY(check_ptr(zeros, "zeros"));
   const awq_config c = cfg ? *cfg : awq_default_config();
-  return launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
-                     reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream),
-                     c.w_bit, c.group, c.zero_point != 0, clip_idx, n_clip);
+  AWQ_TRY(launch_pack(reinterpret_cast<const __half*>(W), s_c, N, K, qweight,
+                      reinterpret_cast<__half*>(scales), zeros, static_cast<cudaStream_t>(stream),
+                      c.w_bit, c.group, c.zero_point != 0, clip_idx, n_clip));
+  return launch_stream_fence(static_cast<cudaStream_t>(stream));
 }
 
 size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K) {

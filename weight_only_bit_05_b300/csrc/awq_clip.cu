@@ -229,12 +229,10 @@ template <int BITS, int GS, bool ZP>
 int launch_search(const __half* W, int N, int K, const float* s_c, const float* H, int n_clip,
                   uint8_t* clip_idx, float* err, cudaStream_t st) {
   const size_t smem = (static_cast<size_t>(GS) * GS + 8 * kCand * GS) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(clip_search_kernel<BITS, GS, ZP>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(smem)));
-    attr_set = true;
+  {
+    const int rc = ensure_smem_attr(reinterpret_cast<const void*>(clip_search_kernel<BITS, GS, ZP>),
+                                    static_cast<int>(smem));
+    if (rc != AWQ_OK) return rc;
   }
   const dim3 grid(K / GS, (N + kRowsPerCta - 1) / kRowsPerCta);
   clip_search_kernel<BITS, GS, ZP><<<grid, 256, smem, st>>>(W, N, K, s_c, H, n_clip, clip_idx,

@@ -118,6 +118,19 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Bulk L2 prefetch of [p, p + bytes) in 8 KB pieces spread over the lanes of
+// the calling warp.  The range is widened to 16-byte boundaries; every buffer
+// the kernel reads starts 16-byte aligned and ends on a 16-byte boundary.
+__device__ __forceinline__ void prefetch_range(const void* p, size_t bytes, int lane) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(15);
+  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~static_cast<uintptr_t>(15);
+  constexpr uintptr_t kPiece = 8192;
+  for (uintptr_t a = a0 + lane * kPiece; a < a1; a += 32 * kPiece) {
+    const uintptr_t e = a + kPiece < a1 ? a + kPiece : a1;
+    prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
+  }
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }

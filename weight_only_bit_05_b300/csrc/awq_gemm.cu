@@ -570,19 +570,13 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
                 float* part = nullptr) {
   using C = Cfg<BN, MODE, BITS>;
   if (kps == 0) kps = K / BK;
-  static bool attr_set = false;
-  if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_kernel<BN, MODE, PERM, BITS>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
-    attr_set = true;
+  {
+    const int rc = ensure_smem_attr(reinterpret_cast<const void*>(gemm_kernel<BN, MODE, PERM, BITS>),
+                                    C::SMEM);
+    if (rc != AWQ_OK) return rc;
   }
   cudaLaunchConfig_t cfg = {};
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    AWQ_CUDA_TRY(cudaGetDevice(&dev));
-    AWQ_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  }
+  const int sms = sm_count();
   const int items = ((N + BM - 1) / BM) * ((M + BN - 1) / BN) * splits;
   cfg.gridDim = dim3(items < sms ? items : sms, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -633,17 +627,6 @@ int pick_bn(int M, int mode) {
 }
 
 }  // namespace
-
-int sm_count() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 148;
-  }
-  return sms;
-}
 
 // Token-tile width and split-K for one launch.  The tile is the smallest of
 // 16..256 tokens that holds M; split-K comes from a cost model in SM cycles:

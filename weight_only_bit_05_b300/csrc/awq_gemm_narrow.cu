@@ -505,11 +505,10 @@ int launch_narrow_tile(const CUtensorMap& tx, const CUtensorMap& tq, const __hal
                        __half* out, int ldo, int splits, int kps, float* part,
                        cudaStream_t st) {
   using C = NCfg<BN, BITS, BKS>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(gemm_narrow_kernel<BN, PERM, BITS, BKS>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
-    attr_set = true;
+  {
+    const int rc = ensure_smem_attr(
+        reinterpret_cast<const void*>(gemm_narrow_kernel<BN, PERM, BITS, BKS>), C::SMEM);
+    if (rc != AWQ_OK) return rc;
   }
   const int sms = sm_count();
   const int items = ((N + NBM - 1) / NBM) * ((M + BN - 1) / BN) * splits;

@@ -102,19 +102,6 @@ __device__ __forceinline__ void word_dot8(uint32_t w, uint32_t zb, uint32_t xa, 
   fma_mixed2(d1, xb, c[2], c[3]);
 }
 
-// Bulk L2 prefetch of [p, p + bytes) in 8 KB pieces spread over the lanes of
-// the calling warp.  The range is widened to 16-byte boundaries; every buffer
-// the kernel reads starts 16-byte aligned and ends on a 16-byte boundary.
-__device__ __forceinline__ void prefetch_range(const void* p, size_t bytes, int lane) {
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(15);
-  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~static_cast<uintptr_t>(15);
-  constexpr uintptr_t kPiece = 8192;
-  for (uintptr_t a = a0 + lane * kPiece; a < a1; a += 32 * kPiece) {
-    const uintptr_t e = a + kPiece < a1 ? a + kPiece : a1;
-    prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
-  }
-}
-
 // MM tokens, R rows per unit, kWarps warps per CTA, MINB CTAs per SM for the
 // register budget.  SILU: the weight stacks I gate rows over I up rows and the
 // kernel writes silu(gate) * up ([M][I]); it walks "virtual" rows v in which
@@ -427,19 +414,6 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   cluster.sync();   // every CTA's shared memory stays alive until rank 0 has read it
 }
 
-int num_sms() {
-  static int cached = -1;
-  if (cached < 0) {
-    int dev = 0, n = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      cached = n;
-    else
-      cached = 148;
-  }
-  return cached;
-}
-
 template <int MM, int R, int kWarps, int MINB, bool SILU, int BITS, int GS>
 int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
                  const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
@@ -465,7 +439,7 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
   const int B = (ks * (128 / CK) + 31) / 32;
   // balancing units: row units, or (gate, up) pairs
   const int units = SILU ? N / 2 : N / R;
-  int gx = num_sms() / nsplit;
+  int gx = sm_count() / nsplit;
   if (gx > units) gx = units;
   if (gx < 1) gx = 1;
   const int rows_cap = ((units + gx - 1) / gx) * (SILU ? 2 : R);
@@ -479,11 +453,9 @@ int launch_shape(const __half* X, const uint32_t* qweight, const __half* scales,
     return AWQ_ERR_SHAPE;
   }
   auto kern = gemv_kernel<MM, R, kWarps, MINB, SILU, BITS, GS>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    AWQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      220 * 1024));
-    attr_set = true;
+  {
+    const int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), 220 * 1024);
+    if (rc != AWQ_OK) return rc;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, nsplit, 1);
@@ -512,7 +484,7 @@ int launch_mm(const __half* X, const uint32_t* qweight, const __half* scales,
     // the half-SM shape for the smallest layers of the default format only
     constexpr bool kDefault = BITS == 4 && GS == 128;
     const size_t code_bytes = static_cast<size_t>(N) * K * BITS / 8;
-    if (kDefault && code_bytes <= kSmallBytesPerSm * num_sms())
+    if (kDefault && code_bytes <= kSmallBytesPerSm * sm_count())
       return launch_shape<MM, 2, 16, 2, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K,
                                                         Y, st);
     return launch_shape<MM, 2, 32, 1, SILU, BITS, GS>(X, qweight, scales, zeros, inv_s, N, K, Y,
@@ -550,6 +522,12 @@ int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* s
       return AWQ_ERR_UNSUPPORTED;
     }
     return launch_m<true, 4, 128>(X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
+  }
+  if (gemv_mma_eligible(M, K, w_bit, group, false)) {
+    const MmaGemvPlan p = plan_gemv_mma(M, N, K, sm_count());
+    if (p.depth > 0)
+      return launch_gemv_mma_plan(p, X, M, qweight, scales, zeros, inv_s, N, K, Y, st);
+    // no shared-memory plan (many tokens on the largest layers): CUDA cores
   }
 #define AWQ_GEMV_CASE(B, GS)                                                              \
   if (w_bit == B && group == GS)                                                          \

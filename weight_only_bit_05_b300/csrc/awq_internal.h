@@ -6,6 +6,13 @@
 
 namespace awq {
 
+// awq_api.cu: per-device launch helpers, safe to call from several host
+// threads.  sm_count: SMs of the current device (148 when it cannot be
+// queried).  ensure_smem_attr: raises the kernel's dynamic shared-memory limit
+// on the current device to at least `bytes` (once per kernel and device).
+int sm_count();
+int ensure_smem_attr(const void* func, int bytes);
+
 // awq_stats.cu
 size_t absmean_workspace_size(int64_t T, int K);
 int launch_absmean(const __half* X, int64_t T, int K, float* a, void* ws, cudaStream_t st);
@@ -22,6 +29,9 @@ int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweig
                 int group = 128, bool zero_point = true, const uint8_t* clip_idx = nullptr,
                 int n_clip = 1);
 
+// Empty non-PDL kernel ending the entry points that write packed weights.
+int launch_stream_fence(cudaStream_t st);
+
 // awq_clip.cu
 size_t clip_workspace_size(int64_t T, int K, int group);
 int launch_clip_search(const __half* X, int64_t T, const __half* W, int N, int K,
@@ -36,6 +46,31 @@ int launch_clip_search(const __half* X, int64_t T, const __half* W, int N, int K
 int launch_gemv(const __half* X, int M, const uint32_t* qweight, const __half* scales,
                 const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
                 cudaStream_t st, bool silu_mul = false, int w_bit = 4, int group = 128);
+
+// awq_gemv_mma.cu: the decode matmul for 4-bit codes in 128-channel groups,
+// M <= 8, K % 256 == 0 (weights streamed by TMA before the dependency wait,
+// dot products on the warp-level MMA).
+struct MmaGemvPlan {
+  int warps;         // warps per CTA, each with its own ring of stages
+  int depth;         // stages per warp ring (0: no plan fits)
+  int nsplit;        // K slices (thread-block cluster size along y)
+  int KS;            // input channels per slice
+  int gx;            // CTAs along the rows
+  int rows_cap;      // most rows of one CTA
+  int smem;          // dynamic shared memory per CTA
+  int ctas_per_sm;   // CTAs of one launch per SM (1 or 2)
+};
+MmaGemvPlan plan_gemv_mma(int M, int N, int K, int sms);
+MmaGemvPlan make_gemv_mma_plan(int M, int N, int K, int sms, int warps, int ctas_per_sm,
+                               int min_depth, int max_depth);
+int launch_gemv_mma_plan(const MmaGemvPlan& p, const __half* X, int M, const uint32_t* qweight,
+                         const __half* scales, const uint32_t* zeros, const float* inv_s, int N,
+                         int K, __half* Y, cudaStream_t st);
+bool gemv_mma_eligible(int M, int K, int w_bit, int group, bool silu_mul);
+int launch_gemv_mma(const __half* X, int M, const uint32_t* qweight, const __half* scales,
+                    const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
+                    cudaStream_t st);
+int read_clear_gemv_error(cudaStream_t st, unsigned* flags);
 
 // awq_fold.cu
 int launch_fold_inv_scales(const __half* W, int64_t rows, int64_t cols, const float* inv_s,
@@ -73,7 +108,6 @@ GemmPlan plan_gemm(int M, int N, int K, int mode);
 size_t gemm_partial_bytes(int M, int N, int K);   // split-K workspace of the plain matmul
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
-int sm_count();   // SMs of the current device (148 when it cannot be queried)
 // Y[m][n] = fp16(sum over s < splits of part[s][m][n]), part fp32 [splits][M][N].
 int launch_splitk_reduce(const float* part, int splits, int M, int N, __half* Y,
                          cudaStream_t st);

@@ -178,4 +178,18 @@ int launch_pack(const __half* W, const float* s_c, int N, int K, uint32_t* qweig
   return AWQ_ERR_UNSUPPORTED;
 }
 
+namespace {
+__global__ void stream_fence_kernel() {}
+}  // namespace
+
+// An empty kernel launched without programmatic dependent launch: it starts
+// only once the kernels before it on the stream have completed and their
+// writes are visible, so a following kernel that reads weights before its
+// dependency wait (the decode matmul) overlaps this kernel, never the pack.
+int launch_stream_fence(cudaStream_t st) {
+  stream_fence_kernel<<<1, 32, 0, st>>>();
+  AWQ_CUDA_TRY_LAUNCH("stream_fence_kernel");
+  return AWQ_OK;
+}
+
 }  // namespace awq
