@@ -326,7 +326,7 @@ def row_errors_gram(H, W16, s_c, inv_s, rows=None, **cfg):
     qw, sc, zs = awq_pack(W16[rows], s_c, **cfg)
     wq = dequant(qw, sc, zs, cfg.get("group", GROUP), cfg.get("w_bit", W_BIT)).astype(np.float64)
     d = wq * np.asarray(inv_s, dtype=np.float64)[None, :] - W16[rows].astype(np.float64)
-    return np.einsum("nk,kj,nj->n", d, H, d)
+    return np.einsum("nk,kj,nj->n", d, H, d, optimize=True)
 
 
 # ------------------------------------- fused projections sharing one input

@@ -96,3 +96,49 @@ def test_clipping_is_chosen_for_an_outlier_weight_on_a_silent_channel():
     idx, err = O.clip_search(X16, w[None, :], None, None, 20)
     assert idx[0, 0] > 0
     assert err[0, 0, idx[0, 0]] < 0.5 * err[0, 0, 0]
+
+
+def test_symmetric_shrunk_range_hand_derived():
+    """Symmetric codes (zero point off, "AWQ量化实战" §3.3) from a range shrunk
+    to r max|w'| (the clipping reading of §5.1), derived by hand.
+
+    4-bit, 32-channel group, n_clip = 4, index 2: r = 1 - 0.5 * 2 / 4 = 0.75.
+    max|w| = 1, so s32 = 0.75 / 7 = 0.107142857... = 1.7142857 * 2^-4; the
+    fp16 mantissa field is round(0.7142857 * 1024) = round(731.43) = 731, so
+    s = (1 + 731/1024) / 16 = 0.10711669921875.  Codes q = clamp(rint(w / s),
+    -8, 7) + 8:  w = -1 -> -9.34 -> -8 -> 0;  1 -> 9.34 -> 7 -> 15;  0.5 ->
+    4.67 -> 5 -> 13;  -0.5 -> 3;  0.25 -> 2.33 -> 2 -> 10;  -0.25 -> 6;
+    0.125 -> 1.17 -> 1 -> 9;  0 -> 8;  0.75 -> 7.0017 -> 7 -> 15;  -0.75 ->
+    1;  0.0625 -> 0.58 -> 1 -> 9;  0.03125 -> 0.29 -> 0 -> 8;  -0.875 ->
+    -8.17 -> -8 -> 0;  0.875 -> 8.17 -> 7 -> 15 (clipped).  Without the
+    shrink (r = 1) the step would be fp16(1/7) = 0.142822265625."""
+    vals = [-1.0, 1.0, 0.5, -0.5, 0.25, -0.25, 0.125, 0.0, 0.75, -0.75, 0.0625, 0.03125,
+            -0.875, 0.875, 0.0, 0.0]
+    codes = [0, 15, 13, 3, 10, 6, 9, 8, 15, 1, 9, 8, 0, 15, 8, 8]
+    w = np.array(vals * 2, dtype=np.float16)[None, :]
+    q, z, s16 = O.quantize_clipped(w, None, np.array([[2]]), 4, group=32, w_bit=4,
+                                   zero_point=False)
+    assert float(s16[0, 0]) == 0.10711669921875
+    assert z[0, 0] == 8
+    assert q[0].tolist() == codes * 2
+    q1, _, s1 = O.quantize_clipped(w, None, np.array([[0]]), 4, group=32, w_bit=4,
+                                   zero_point=False)
+    assert float(s1[0, 0]) == 0.142822265625
+
+
+def test_symmetric_shrunk_range_hand_derived_8bit():
+    """8-bit symmetric, 32-channel group, n_clip = 10, index 4: r = fp32(0.8).
+    max|w| = 1 gives s32 = 0.8 / 127 = 0.0062992 = 1.6125984 * 2^-8; mantissa
+    field round(0.6125984 * 1024) = round(627.30) = 627, so s = (1 + 627/1024)
+    / 256 = 0.006298065185546875.  Codes q = clamp(rint(w / s), -128, 127) +
+    128:  1 -> 158.8 -> 127 -> 255 (clipped);  0.5 -> 79.4 -> 79 -> 207;
+    -0.25 -> -39.7 -> -40 -> 88;  fp16(0.1) = 0.0999755859375 -> 15.87 -> 16
+    -> 144;  -1 -> -158.8 -> -128 -> 0;  0 -> 128."""
+    vals = [1.0, 0.5, -0.25, 0.1, -1.0, 0.0, 0.0, 0.0]
+    codes = [255, 207, 88, 144, 0, 128, 128, 128]
+    w = np.array(vals * 4, dtype=np.float16)[None, :]
+    q, z, s16 = O.quantize_clipped(w, None, np.array([[4]]), 10, group=32, w_bit=8,
+                                   zero_point=False)
+    assert float(s16[0, 0]) == 0.006298065185546875
+    assert z[0, 0] == 128
+    assert q[0].tolist() == codes * 4
