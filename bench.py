@@ -42,13 +42,13 @@ SHAPES = ["qkv", "o", "gate_up", "down"]
 PREFILL = [("llama2-7b", s) for s in SHAPES] + [("llama2-13b", s) for s in SHAPES]
 METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofline"
 
-# DRAM bytes (read + write) per launch of the GEMV on each 7B decode shape, from
-# one ncu capture (profiles/gemv_kernel_7b_decode.md).  They are reported only
-# while the kernel source is byte-identical to the one that was captured.
+# DRAM bytes (read + write) per launch of the decode GEMV on each 7B shape, from
+# one ncu capture of this script (--layers 2).  They are reported only while the
+# kernel source is byte-identical to the one that was captured.
 GEMV_TRAFFIC = {
-    "source": "weight_only_bit_05_b300/csrc/awq_gemv.cu",
-    "sha256": "166c2f6c4a714d587403d94766379a75f3d271dc1ac41276a7ea7c6b8f8a383d",
-    "per_launch": {"qkv": 26214912, "o": 8781824, "gate_up": 46918912, "down": 23536896},
+    "source": "weight_only_bit_05_b300/csrc/awq_gemv_mma.cu",
+    "sha256": "6b4b21fd0ee7f3399476ca3281bdc3b0a6c284b2f6c90cfbb0b3bfffc52abd31",
+    "per_launch": {"qkv": 26229504, "o": 8796672, "gate_up": 46940928, "down": 23550720},
 }
 
 
@@ -57,7 +57,8 @@ def gemv_traffic():
     ``roofline.achieved``), or None when the kernel changed since the capture."""
     import hashlib
     with open(os.path.join(ROOT, GEMV_TRAFFIC["source"]), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != GEMV_TRAFFIC["sha256"]:
+        if hashlib.sha256(f.read()).hexdigest() != GEMV_TRAFFIC["sha256"] or \
+                not GEMV_TRAFFIC["per_launch"]:
             return None, None
     per = GEMV_TRAFFIC["per_launch"]
     return round(sum(per.values()) / len(per)), dict(per)
@@ -80,10 +81,45 @@ def peaks():
 
 
 # ----------------------------------------------------------------- clocks
+class _NvmlC:
+    """Read-only NVML through ctypes (libnvidia-ml.so.1 of the driver): SM
+    clock, its maximum and the clock-event reasons of one device."""
+
+    def __init__(self, bus, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        rc = (self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h))
+              if bus else self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)))
+        if rc != 0:
+            raise RuntimeError(f"NVML device handle: error {rc}")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self):
+        c = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(c))   # NVML_CLOCK_SM
+        return c.value
+
+    def sm_max(self):
+        c = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(c))
+        return c.value
+
+    def reasons(self):
+        r = self.ct.c_ulonglong()
+        self._reasons(self.h, self.ct.byref(r))
+        return r.value
+
+
 class ClockSampler:
     """Samples the SM clock and the clock-event reasons during the timed
-    region: through NVML when pynvml is importable, else by running
-    ``nvidia-smi --query-gpu ... -lms 50`` in the background."""
+    region every ~1 ms: through NVML (pynvml, else the driver's
+    libnvidia-ml.so.1 through ctypes), else by running ``nvidia-smi
+    --query-gpu ... -lms 50`` in the background.  Read-only."""
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     NAMES = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
              0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
@@ -102,30 +138,38 @@ class ClockSampler:
         try:
             import pynvml as nv
             nv.nvmlInit()
-            self.nv = nv
-            self.h = (nv.nvmlDeviceGetHandleByPciBusId(self.bus) if self.bus
-                      else nv.nvmlDeviceGetHandleByIndex(int(torch_dev)))
-            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            h = (nv.nvmlDeviceGetHandleByPciBusId(self.bus) if self.bus
+                 else nv.nvmlDeviceGetHandleByIndex(int(torch_dev)))
+            self.read = (lambda: nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM),
+                         lambda: nv.nvmlDeviceGetCurrentClocksEventReasons(h))
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
             self.mode = "nvml"
         except Exception as e:
-            self.err = repr(e)[:120]
-            self.mode = "smi"
+            self.err = repr(e)[:100]
+            try:
+                c = _NvmlC(self.bus, int(torch_dev))
+                self.read = (c.sm_clock, c.reasons)
+                self.max_mhz = c.sm_max()
+                self.mode = "nvml-ctypes"
+            except Exception as e2:
+                self.err += " / " + repr(e2)[:100]
+                self.mode = "smi"
 
     def _run_nvml(self):
-        nv = self.nv
+        clock, reasons = self.read
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append(clock())
+                r = reasons()
                 for bit, name in self.NAMES.items():
                     if r & bit:
                         self.reasons.add(name)
             except Exception:
                 pass
-            time.sleep(0.002)
+            time.sleep(0.001)
 
     def __enter__(self):
-        if self.mode == "nvml":
+        if self.mode in ("nvml", "nvml-ctypes"):
             self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
         else:
@@ -144,7 +188,7 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
-        if self.mode == "nvml":
+        if self.mode in ("nvml", "nvml-ctypes"):
             self._stop.set()
             self.t.join()
         elif getattr(self, "proc", None) is not None:
@@ -461,23 +505,27 @@ BATCHED_M = (8, 32, 128)
 
 
 def batched_7b(awq, torch, hbm, pk, reps=10):
-    """The Llama-2-7B shapes as batched decode, M = 8 / 32 / 128: awq_gemv at
-    M = 8 and awq_gemm at every M, over rotating weight copies (weights do
-    not stay in L2); GB/s of the algorithmic bytes and TFLOP/s of 2 M N K."""
+    """The Llama-2-7B shapes as batched decode, M = 8 / 32 / 128: W ~ N(0,
+    0.02) quantized with the AWQ scales that awq_search_scales picks on 4096
+    synthetic calibration tokens with 1% outlier channels, then awq_gemv at
+    M = 8 and awq_gemm at every M on tokens of the same distribution, over
+    rotating weight copies (weights do not stay in L2); GB/s of the
+    algorithmic bytes and TFLOP/s of 2 M N K."""
     dev = torch.device("cuda")
-    gen = torch.Generator(device=dev)
     peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
     out = {}
     for name in ("qkv", "o", "gate_up", "down"):
         K, N, lid = awq_inputs.layer(MODEL, name)
-        gen.manual_seed(1000 + lid)
-        qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
-        inv_s = torch.ones(K, dtype=torch.float32, device=dev)
+        W = torch.from_numpy(awq_inputs.weight(N, K, lid)).to(dev)
+        res = awq.search(torch.from_numpy(awq_inputs.calib_tokens(4096, K, lid)).to(dev), W)
+        inv_s = res["inv_s"]
+        qw, sc, zs = awq.pack(W, res["s_c"])
+        del W
         ncp = max(4, -(-3 * 126 * 2**20 // gemv_bytes(1, N, K)))
         copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(ncp - 1)]
-        row = {}
+        row = {"alpha": res["alpha"]}
         for M in BATCHED_M:
-            X = torch.randn((M, K), generator=gen, device=dev).half()
+            X = torch.from_numpy(awq_inputs.timed_tokens(M, K, lid)).to(dev)
             Y = torch.empty((M, N), dtype=torch.float16, device=dev)
             ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
             fns = [("gemm", lambda X=X, Y=Y, ws=ws: [awq.gemm(X, q, s_, z, inv_s, out=Y, workspace=ws)
@@ -516,7 +564,9 @@ SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
 def sweep_70b(awq, torch, hbm, pk, reps=5):
     """The Llama-2-70B layers over the token count M: awq_gemv for M = 1,
     both awq_gemv and awq_gemm for M = 2, 4 and 8 (keys "M4 gemv", "M4 gemm"),
-    awq_gemm above; GB/s of the algorithmic bytes and TFLOP/s of 2 M N K."""
+    awq_gemm above; every launch over rotating weight copies of at least 3x
+    the L2 in total (so every M reads its weights from HBM); GB/s of the
+    algorithmic bytes and TFLOP/s of 2 M N K."""
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
     peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
@@ -526,16 +576,19 @@ def sweep_70b(awq, torch, hbm, pk, reps=5):
         gen.manual_seed(1000 + lid)
         qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device=dev) * 0.02).half())
         inv_s = torch.ones(K, dtype=torch.float32, device=dev)
-        row = {}
+        ncp = max(2, -(-3 * 126 * 2**20 // gemv_bytes(1, N, K)))
+        copies = [(qw, sc, zs)] + [(qw.clone(), sc.clone(), zs.clone()) for _ in range(ncp - 1)]
+        row = {"copies": ncp}
         for M, kind in [(m, k) for m in SWEEP_M
                         for k in (("gemv",) if m == 1 else ("gemv", "gemm") if m <= 8 else ("gemm",))]:
             X = torch.randn((M, K), generator=gen, device=dev).half()
             Y = torch.empty((M, N), dtype=torch.float16, device=dev)
             if kind == "gemv":
-                fn = lambda X=X, Y=Y: awq.gemv(X, qw, sc, zs, inv_s, out=Y)
+                fn = lambda X=X, Y=Y: [awq.gemv(X, q, s_, z, inv_s, out=Y) for q, s_, z in copies]
             else:
                 ws = torch.empty(awq.gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
-                fn = lambda X=X, Y=Y, ws=ws: awq.gemm(X, qw, sc, zs, inv_s, out=Y, workspace=ws)
+                fn = lambda X=X, Y=Y, ws=ws: [awq.gemm(X, q, s_, z, inv_s, out=Y, workspace=ws)
+                                              for q, s_, z in copies]
             g = capture(torch, fn)
             for _ in range(3):
                 g.replay()
@@ -546,18 +599,17 @@ def sweep_70b(awq, torch, hbm, pk, reps=5):
                 g.replay()
             e1.record()
             torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1000 / reps
+            us = e0.elapsed_time(e1) * 1000 / (reps * ncp)
             gbs = gemv_bytes(M, N, K) / us / 1e3
             tf = 2.0 * M * N * K / us / 1e6
             key = f"M{M} {kind}" if 1 < M <= 8 else f"M{M}"
             row[key] = {"us": round(us, 1), "GB/s": round(gbs, 1), "TFLOP/s": round(tf, 1),
-                            "hbm_frac": round(gbs / hbm, 3), "tensor_frac": round(tf / peak, 3)}
+                        "hbm_frac": round(gbs / hbm, 3), "tensor_frac": round(tf / peak, 3)}
             del g, X, Y
         out[f"{name} {K}->{N}"] = row
-        del qw, sc, zs
+        del copies, qw, sc, zs
         torch.cuda.empty_cache()
-    return {"note": "weights of one layer, L2-resident for the small ones: an upper bound on "
-                    "decode GB/s, exact for the tensor-bound M", "layers": out}
+    return {"note": "weights rotated over copies of >= 3x L2 at every M", "layers": out}
 
 
 def clip_run(awq, torch, model=MODEL, name="qkv", T=4096, n_clip=20):
@@ -656,6 +708,54 @@ def search_run(awq, torch, model="llama2-70b", name="gate_up", T=65536):
             "seconds": round(dt, 3), "tflops": round(flop / dt / 1e12, 1),
             "alpha": res["alpha"], "includes": "statistics, 20x (pack, prescale, squared-error "
                                                "GEMM, reductions), Y_ref GEMM, host argmin"}
+
+
+def summarize(line, hbm):
+    """One figure and one roofline fraction per configuration, scalars only
+    (the last key of the JSON line, so that a record that keeps only the end
+    of the line still holds every configuration)."""
+    out = {"decode_7b_M1_GB/s": line["value"], "decode_7b_M1_frac": line["roofline"]["frac"],
+           "decode_7b_ceiling_frac": round(line["roofline"]["step_ceiling_GB/s"] / hbm, 4),
+           "decode_7b_e2e_GB/s": line["e2e"]["value"]}
+    g70 = line.get("gemv_70b")
+    if g70:
+        for k, v in g70.items():
+            out[f"gemv70b_{k.split()[0]}_frac"] = v["frac"]
+    b7 = line.get("batched_7b")
+    if b7:
+        for M in BATCHED_M:
+            fr = [r[f"M{M} gemm"]["hbm_frac"] for r in b7.values()]
+            tf = [r[f"M{M} gemm"]["TFLOP/s"] for r in b7.values()]
+            out[f"batched7b_M{M}_hbm_frac_min"] = min(fr)
+            out[f"batched7b_M{M}_hbm_frac_max"] = max(fr)
+            out[f"batched7b_M{M}_tflops_max"] = max(tf)
+        out["batched7b_M8_gemv_hbm_frac_min"] = min(r["M8 gemv"]["hbm_frac"] for r in b7.values())
+    sw = line.get("sweep_70b")
+    if sw:
+        for lo, hi, tag in ((1, 8, "M1-8"), (16, 64, "M16-64"), (128, 512, "M128-512"),
+                            (1024, 4096, "M1024-4096")):
+            hb, tf = [], []
+            for r in sw["layers"].values():
+                for k, v in r.items():
+                    if not k.startswith("M"):
+                        continue
+                    m = int(k.split()[0][1:])
+                    if lo <= m <= hi:
+                        hb.append(v["hbm_frac"])
+                        tf.append(v["tensor_frac"])
+            out[f"sweep70b_{tag}_hbm_frac_best"] = max(hb)
+            out[f"sweep70b_{tag}_tensor_frac_best"] = max(tf)
+    gp = line.get("gemm_prefill")
+    if gp:
+        out["prefill_tflops"] = gp["tflops"]
+        out["prefill_frac"] = gp["frac"]
+        out["prefill_frac_min_shape"] = round(min(gp["per_shape_tflops"].values()) /
+                                              gp["peak_tflops"], 4)
+    se = line.get("search")
+    if se:
+        out["search70b_s"] = se["seconds"]
+        out["search70b_tflops"] = se["tflops"]
+    return out
 
 
 def replica_value(torch, ms_local, world, step_bytes, steps, device):
@@ -798,6 +898,33 @@ def main():
         del g
     achieved = tot_b / tot_ms / 1e3
 
+    # ceiling of the same chain: a plain streaming read of each launch's
+    # weight buffers (codes, steps, zero points) in the same 128-launch graph
+    # with the same programmatic dependent launch, reading after the
+    # dependency wait (a plain chain) and before it (as the GEMV does)
+    sink = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    ceiling = {}
+    for read_first in (0, 1):
+        def sread(read_first=read_first):
+            for X, qw, sc, zs, inv_s, Y, _ in calls:
+                for buf in (qw, sc, zs):
+                    awq.measure_stream_read(buf, read_first, sink)
+        g = capture(torch, sread)
+        g.replay()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, min(20, args.steps))
+        c0.record()
+        for _ in range(reps):
+            g.replay()
+        c1.record()
+        torch.cuda.synchronize()
+        wbytes = sum(c[1].numel() * 4 + c[2].numel() * 2 + c[3].numel() * 4 for c in calls)
+        gbs = wbytes / (c0.elapsed_time(c1) / reps / 1000) / 1e9
+        ceiling["read_before_wait" if read_first else "read_after_wait"] = {
+            "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+        del g
+    ceil_best = max(v["GB/s"] for v in ceiling.values())
+
     # end to end through the public API: host inputs in, host outputs out, every step
     xh = torch.empty(Xall.shape, dtype=Xall.dtype, pin_memory=True)
     xh.copy_(Xall)
@@ -851,14 +978,17 @@ def main():
                          f"({step_bytes / 1e9:.2f} GB per step vs 126 MB L2)",
                    "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events",
                    "extra_warmup_steps": extra},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": traffic,
-                     "traffic_per_shape": traffic_shape,
-                     "algorithmic_bytes_per_launch": round(tot_b / len(shapes)),
-                     "frac_of_8tbs_spec": round(achieved / 8000.0, 4),
-                     "kernel": "gemv_kernel<1> (awq_gemv)", "peak_kind": pk_kind,
-                     "per_shape": per_shape,
-                     "bytes_per_launch": {s["name"]: s["bytes"] for s in shapes}},
+        "roofline": dict({"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                          "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                          "algorithmic_bytes_per_launch": round(tot_b / len(shapes)),
+                          "frac_of_8tbs_spec": round(achieved / 8000.0, 4),
+                          "kernel": "gemv_mma_kernel (awq_gemv)", "peak_kind": pk_kind,
+                          "step_ceiling_GB/s": ceil_best,
+                          "step_frac_of_ceiling": round(value / ceil_best, 4),
+                          "traffic_per_shape": traffic_shape, "per_shape": per_shape,
+                          "ceiling": ceiling},
+                         **{f"us_{k}": v["us_per_launch"] for k, v in per_shape.items()},
+                         **{f"frac_{k}": round(v["GB/s"] / hbm, 4) for k, v in per_shape.items()}),
         "clocks": clk.summary(),
         "gpu_launches": args.steps * len(calls),
         "e2e": e2e,
@@ -873,6 +1003,7 @@ def main():
         "gemm_prefill": gemm,
         "search": search,
     }
+    line["summary"] = summarize(line, hbm)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

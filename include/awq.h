@@ -283,6 +283,19 @@ AWQ_API int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* 
                       float* inv_s_out, int32_t* best_out, double* mse_out,
                       double* row_err_out, void* stream);
 
+/* --------------------------------------------------------- measurement aid
+ * Not a step of the method (the pages have no counterpart): a plain streaming
+ * read of `bytes` bytes at `buf` (device, 16-byte aligned, bytes a multiple of
+ * 16), launched like awq_gemv with programmatic dependent launch, one CTA per
+ * SM. A chain of these over the same weight buffers as a chain of awq_gemv
+ * calls measures the bandwidth ceiling that HBM and the overlap of
+ * consecutive launches leave such a chain. read_first != 0 issues the reads
+ * before waiting for the previous kernel in the stream (as awq_gemv does with
+ * its weights), 0 after. `out`: device, one uint32 per SM, written only when
+ * the buffer's words fold to one particular value. */
+AWQ_API int awq_measure_stream_read(const void* buf, size_t bytes, int32_t read_first,
+                                    uint32_t* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,8 @@ import torch
 
 __all__ = ["lib", "LIB_PATH", "AwqError", "exported_symbols", "absmean", "channel_scales", "pack",
            "gemv", "gemm", "search", "check_device_error", "gemm_workspace_bytes",
-           "gemv_silu_mul", "gemm_silu_mul", "fold_inv_scales", "clip_search", "pack_clipped"]
+           "gemv_silu_mul", "gemm_silu_mul", "fold_inv_scales", "clip_search", "pack_clipped",
+           "measure_stream_read"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libawq.so")
@@ -70,6 +71,7 @@ _SIGS = {
                                        ctypes.POINTER(AwqConfig), _i32, _p, _sz, _p, _p, _p]),
     "awq_pack_clipped": (ctypes.c_int, [_p, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p, _i32,
                                         _p, _p, _p, _p]),
+    "awq_measure_stream_read": (ctypes.c_int, [_p, _sz, _i32, _p, _p]),
     "awq_search_workspace_size": (_sz, [_i64, _i32, _i32]),
     "awq_search_scales": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p,
                                          _sz, _p, _p, ctypes.POINTER(ctypes.c_int32),
@@ -321,3 +323,13 @@ def search(X_cal: torch.Tensor, W: torch.Tensor, n_grid: int = 20, row_err: bool
                                  _ptr(rerr), _stream()))
     return {"best": best.value, "alpha": best.value / n_grid, "mse": list(mse), "s_c": s_c,
             "inv_s": inv_s, "row_err": rerr}
+
+
+def measure_stream_read(buf: torch.Tensor, read_first: bool, out: torch.Tensor):
+    """Measurement aid: one streaming read of ``buf`` (any contiguous CUDA
+    tensor, size a multiple of 16 bytes) launched like :func:`gemv`; ``out``
+    is an int32 CUDA tensor with one element per SM."""
+    if not (buf.is_cuda and buf.is_contiguous() and out.is_cuda and out.dtype == torch.int32):
+        raise ValueError("buf and out must be contiguous CUDA tensors, out int32")
+    _check(lib.awq_measure_stream_read(_ptr(buf), buf.numel() * buf.element_size(),
+                                       int(bool(read_first)), _ptr(out), _stream()))

@@ -452,4 +452,15 @@ int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
                      workspace, ws_bytes, stream);
 }
 
+int awq_measure_stream_read(const void* buf, size_t bytes, int32_t read_first, uint32_t* out,
+                            void* stream) {
+  if (bytes == 0 || bytes % 16 != 0) {
+    set_error("awq_measure_stream_read: bytes = %zu must be a positive multiple of 16", bytes);
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(check_ptr(buf, "buf"));
+  AWQ_TRY(check_ptr(out, "out"));
+  return launch_stream_read(buf, bytes, read_first, out, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

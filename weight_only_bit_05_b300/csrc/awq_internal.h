@@ -72,6 +72,12 @@ int launch_gemv_mma(const __half* X, int M, const uint32_t* qweight, const __hal
                     cudaStream_t st);
 int read_clear_gemv_error(cudaStream_t st, unsigned* flags);
 
+// awq_measure.cu: streaming read of `bytes` (a multiple of 16) for the
+// bandwidth ceiling of a chain of launches; `out` receives nothing unless the
+// buffer folds to one particular word (one word per SM must be writable).
+int launch_stream_read(const void* buf, size_t bytes, int read_first, unsigned* out,
+                       cudaStream_t st);
+
 // awq_fold.cu
 int launch_fold_inv_scales(const __half* W, int64_t rows, int64_t cols, const float* inv_s,
                            __half* out, cudaStream_t st);
