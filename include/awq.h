@@ -91,9 +91,15 @@ AWQ_API awq_config awq_default_config(void);
 /* Human-readable reason of the last failing call on this host thread. */
 AWQ_API const char* awq_last_error_string(void);
 
-/* Reads and clears the device-side error word of the kernels that use bounded
- * waits (the tensor-core matmul). Synchronizes `stream`. Returns AWQ_OK if no
- * kernel reported a timeout since the last call, AWQ_ERR_DEVICE otherwise. */
+/* Reads and clears the device-side error words of the kernels that use
+ * bounded waits (the tensor-core matmuls and the decode matmul): every wait on
+ * an mbarrier gives up after a limit (1 s) instead of hanging, records the
+ * fact in a word of the current device, lets its copies in flight land and
+ * returns; the output of that call is then undefined. The words are per
+ * device and shared by all streams and host threads, so this call first
+ * synchronizes the whole current device (`stream` is not used beyond that)
+ * and reports a timeout of any call on the device since the last check.
+ * Returns AWQ_OK if none, AWQ_ERR_DEVICE otherwise. */
 AWQ_API int awq_check_device_error(void* stream);
 
 /* ---------------------------------------------------------------- statistics
@@ -282,6 +288,22 @@ AWQ_API int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* 
                       void* workspace, size_t ws_bytes, float* s_c_out,
                       float* inv_s_out, int32_t* best_out, double* mse_out,
                       double* row_err_out, void* stream);
+
+/* --------------------------------------------------------------- test hook
+ * Not a step of the method (the pages have no counterpart): lets a test drive
+ * the bounded waits to expiry without faulting or hanging the GPU.
+ * `which` selects the kernels whose following launches on the current device
+ * lose one copy: bit 0 (1) the decode matmul of awq_gemv's default format
+ * (the first CTA does not request its first stage), bit 1 (2) the
+ * wide tensor-core matmul of awq_gemm, M > 128 (the producer of the first CTA
+ * does not request its first stage). The wait for that stage runs out after
+ * wait_limit_ns, the kernel records it for awq_check_device_error, stops its
+ * other roles, waits (bounded) for its copies and MMAs in flight, frees its
+ * tensor memory and returns; that call's Y is undefined. wait_limit_ns (1e3 ..
+ * 1e10) becomes the limit of every bounded wait of both kernels.
+ * awq_debug_stall(0, 1000000000) restores the defaults. Device-wide state:
+ * not for concurrent use. */
+AWQ_API int awq_debug_stall(int32_t which, int64_t wait_limit_ns);
 
 /* --------------------------------------------------------- measurement aid
  * Not a step of the method (the pages have no counterpart): a plain streaming

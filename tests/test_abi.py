@@ -143,3 +143,11 @@ def test_variant_configs_are_accepted_by_validation():
     bad.w_bit = 3
     assert lib.awq_gemm_ex(ctypes.byref(bad), FAKE, 4, FAKE, FAKE, FAKE, None, 512, 512, FAKE,
                            None, 0, None) == AWQ_ERR_UNSUPPORTED
+
+
+def test_debug_stall_hook_validates_its_arguments():
+    """The test hook rejects a kernel selection outside 0..3 and a wait limit
+    outside [1e3, 1e10] ns before any CUDA call (runs without a GPU)."""
+    for which, ns in ((1, 0), (1, 999), (2, 10_000_000_001), (4, 1_000_000), (-1, 1_000_000)):
+        assert awq.lib.awq_debug_stall(which, ns) == 1   # AWQ_ERR_SHAPE
+        assert b"awq_debug_stall" in awq.lib.awq_last_error_string()

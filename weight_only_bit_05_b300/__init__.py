@@ -29,7 +29,7 @@ import torch
 __all__ = ["lib", "LIB_PATH", "AwqError", "exported_symbols", "absmean", "channel_scales", "pack",
            "gemv", "gemm", "search", "check_device_error", "gemm_workspace_bytes",
            "gemv_silu_mul", "gemm_silu_mul", "fold_inv_scales", "clip_search", "pack_clipped",
-           "measure_stream_read"]
+           "measure_stream_read", "debug_stall"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libawq.so")
@@ -72,6 +72,7 @@ _SIGS = {
     "awq_pack_clipped": (ctypes.c_int, [_p, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p, _i32,
                                         _p, _p, _p, _p]),
     "awq_measure_stream_read": (ctypes.c_int, [_p, _sz, _i32, _p, _p]),
+    "awq_debug_stall": (ctypes.c_int, [_i32, _i64]),
     "awq_search_workspace_size": (_sz, [_i64, _i32, _i32]),
     "awq_search_scales": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, ctypes.POINTER(AwqConfig), _p,
                                          _sz, _p, _p, ctypes.POINTER(ctypes.c_int32),
@@ -333,3 +334,11 @@ def measure_stream_read(buf: torch.Tensor, read_first: bool, out: torch.Tensor):
         raise ValueError("buf and out must be contiguous CUDA tensors, out int32")
     _check(lib.awq_measure_stream_read(_ptr(buf), buf.numel() * buf.element_size(),
                                        int(bool(read_first)), _ptr(out), _stream()))
+
+
+def debug_stall(which: int, wait_limit_ns: int = 1_000_000_000):
+    """Test hook: ``which`` 1 (awq_gemv), 2 (awq_gemm, M > 128) or 3 makes the
+    next launches of those kernels lose one stage's copy, so that a bounded
+    wait runs out after ``wait_limit_ns`` (see awq.h); ``debug_stall(0)``
+    restores the defaults."""
+    _check(lib.awq_debug_stall(int(which), int(wait_limit_ns)))

@@ -172,6 +172,8 @@ awq_config awq_default_config(void) {
 const char* awq_last_error_string(void) { return g_err; }
 
 int awq_check_device_error(void* stream) {
+  // every stream's kernels report into the same per-device words
+  AWQ_CUDA_TRY(cudaDeviceSynchronize());
   unsigned flags = 0;
   AWQ_TRY(read_clear_gemm_error(static_cast<cudaStream_t>(stream), &flags));
   unsigned narrow = 0;
@@ -450,6 +452,20 @@ int awq_gemm_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
   }
   return gemm_common(kGemmSiluF16, nullptr, X, M, qweight, scales, zeros, inv_s, 2 * I, K, Y, I,
                      workspace, ws_bytes, stream);
+}
+
+int awq_debug_stall(int32_t which, int64_t wait_limit_ns) {
+  if (which < 0 || which > 3) {
+    set_error("awq_debug_stall: which = %d must be a combination of 1 and 2", which);
+    return AWQ_ERR_SHAPE;
+  }
+  if (wait_limit_ns < 1000 || wait_limit_ns > 10000000000ll) {
+    set_error("awq_debug_stall: wait_limit_ns = %lld must be in [1e3, 1e10]",
+              static_cast<long long>(wait_limit_ns));
+    return AWQ_ERR_SHAPE;
+  }
+  AWQ_TRY(set_gemv_stall(which & 1, static_cast<uint64_t>(wait_limit_ns)));
+  return set_gemm_stall(which & 2, static_cast<uint64_t>(wait_limit_ns));
 }
 
 int awq_measure_stream_read(const void* buf, size_t bytes, int32_t read_first, uint32_t* out,

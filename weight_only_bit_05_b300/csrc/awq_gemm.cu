@@ -36,6 +36,10 @@
 namespace awq {
 
 __device__ unsigned int g_gemm_error = 0;
+// Test hook (awq_debug_stall): the limit of every bounded wait, and a request
+// that the producer of the first CTA withhold the copies of its first stage.
+__device__ unsigned long long g_gemm_wait_ns = 1000000000ull;
+__device__ unsigned int g_gemm_withhold = 0;
 
 namespace {
 
@@ -44,7 +48,10 @@ constexpr int BK = 64;           // K per stage: one 128-byte swizzle atom of fp
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * (kDeqWarps + kEpiWarps);
-constexpr uint64_t kWaitNs = 1000000000ull;
+// limit of the bounded waits, read only on their slow path
+__device__ __forceinline__ uint64_t wait_limit_ns() {
+  return *const_cast<volatile unsigned long long*>(&g_gemm_wait_ns);
+}
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
 template <int BN, int MODE, int BITS>
@@ -78,7 +85,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (ab.raised()) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) {
+    if (globaltimer_ns() - t0 > wait_limit_ns()) {
       ab.raise(bit);
       return false;
     }
@@ -235,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;   // k-blocks issued by this CTA over all its tiles
       bool ok = true;
+      // test hook: the first stage of the first CTA is never requested
+      const bool withhold = g_gemm_withhold != 0 && blockIdx.x == 0;
       for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
         const int tile = t / splits;
         const int n0 = (tile % n_tiles) * BM, m0 = (tile / n_tiles) * BN;
@@ -246,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (it == 0 && withhold) continue;
           mbar_arrive_expect_tx(full + s, (MODE == kGemmDenseF32 ? C::A_BYTES : C::RAW_BYTES) +
                                               C::B_BYTES);
           if (MODE == kGemmDenseF32)
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % S;
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(full + s, (j / S) & 1))
-          if (globaltimer_ns() - t0 > kWaitNs) {
+          if (globaltimer_ns() - t0 > wait_limit_ns()) {
             ab.raise(16u);
             break;
           }
@@ -307,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0))
-        if (globaltimer_ns() - t0 > kWaitNs) {
+        if (globaltimer_ns() - t0 > wait_limit_ns()) {
           ab.raise(32u);
           break;
         }
@@ -796,6 +806,14 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
                                ldo, yref, ldy, st, plan.splits, plan.kps, part);
   return launch_gemm_bits<4>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
                              ldo, yref, ldy, st, plan.splits, plan.kps, part);
+}
+
+int set_gemm_stall(int withhold, uint64_t wait_ns) {
+  const unsigned w = withhold ? 1u : 0u;
+  const unsigned long long ns = wait_ns;
+  AWQ_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_withhold, &w, sizeof(w)));
+  AWQ_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_wait_ns, &ns, sizeof(ns)));
+  return AWQ_OK;
 }
 
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags) {

@@ -52,6 +52,11 @@ namespace cg = cooperative_groups;
 namespace awq {
 
 __device__ unsigned int g_gemv_error = 0;
+// Test hook (awq_debug_stall): the limit of every bounded wait, and a request
+// that the first CTA withhold the TMA of its first stage, so that the wait
+// for that stage runs out.
+__device__ unsigned long long g_gemv_wait_ns = 1000000000ull;
+__device__ unsigned int g_gemv_withhold = 0;
 
 namespace {
 
@@ -59,7 +64,6 @@ constexpr int kStageK = 512;                      // input channels per stage
 constexpr int kBoxBytes = 16 * 128;               // 16 rows x 32 words
 constexpr int kStageBytes = 2 * kBoxBytes;        // codes of one stage
 constexpr int kSideBytes = 16 * 8 + 16 * 4;       // steps [16][4] fp16, zero words [16]
-constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr int kMaxDepth = 8;
 // Shared memory of one CTA when two CTAs share an SM (228 KB per SM, 1 KB
 // reserved per CTA), and when one CTA has the SM.
@@ -95,6 +99,14 @@ __device__ __forceinline__ void mma16816_first(float (&d)[4], uint32_t a0, uint3
       "{%8,%9}, {%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Bounded wait on a phase of `bar`; the limit is read only once the first
+// test has failed (the hot path keeps no register for it).  False when the
+// limit ran out.
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_bounded(bar, parity, *const_cast<volatile unsigned long long*>(&g_gemv_wait_ns));
 }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -186,14 +198,15 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     z_src = (lane < 16 && pz >= 0) ? zeros + static_cast<size_t>(pz) * ZW : nullptr;
   };
   set_tile();
-  // Issues the stage at the cursor into its slot and advances the cursor.
-  auto issue = [&]() {
+  // Issues the stage at the cursor into its slot and advances the cursor;
+  // withhold (the test hook only): the stage's codes are never requested.
+  auto issue = [&](bool withhold) {
     const int kc = kbeg + ij * kStageK;
     const bool full = kbeg + klen - kc >= kStageK;       // 4 groups, else 2
     uint8_t* cb = my_codes + islot * kStageBytes;
     uint8_t* sd = my_side + islot * kSideBytes;
     uint64_t* bar = my_bars + islot;
-    if (elect_one()) {
+    if (!withhold && elect_one()) {
       mbar_arrive_expect_tx(bar, full ? 2 * kBoxBytes : kBoxBytes);
       tma_load_2d(cb, &tq, bar, kc >> 3, its);
       if (full) tma_load_2d(cb + kBoxBytes, &tq, bar, (kc >> 3) + 32, its);
@@ -219,7 +232,15 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     if (warp == 0) prefetch_tmap(&tq);
   }
   __syncwarp();
-  while (next < se && next < sb + depth) issue();
+  {
+    // the warp whose run holds the first stage of the first CTA
+    bool withhold = g_gemv_withhold != 0 && blockIdx.x == 0 && blockIdx.y == 0 && sb == 0 &&
+                    se > 0;
+    while (next < se && next < sb + depth) {
+      issue(withhold);
+      withhold = false;
+    }
+  }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // One CTA per SM: the next launch's CTAs can only start where one of this
@@ -307,7 +328,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   int ct = tf, cj = sb - tf * C, cslot = 0;
   uint32_t cphase = 0;
   for (int i = sb; i < se; ++i) {
-    if (!mbar_wait_bounded(my_bars + cslot, cphase, kWaitNs)) {
+    if (!wait_stage(my_bars + cslot, cphase)) {
       if (lane == 0) atomicOr(&g_gemv_error, 1u);
       failed_at = i;
       break;
@@ -378,7 +399,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     __syncwarp();
     if (next < se) {
       fence_proxy_async_smem();
-      issue();
+      issue(false);
     }
     if (!triggered && next >= se) {
       asm volatile("griddepcontrol.launch_dependents;");
@@ -400,7 +421,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     // drain the copies still in flight into this warp's ring (bounded): the
     // stages failed_at .. next - 1 are in the slots from cslot on
     for (int i = failed_at; i < next; ++i) {
-      mbar_wait_bounded(my_bars + cslot, cphase, kWaitNs);
+      wait_stage(my_bars + cslot, cphase);
       if (++cslot == depth) {
         cslot = 0;
         cphase ^= 1u;
@@ -570,6 +591,14 @@ int launch_gemv_mma(const __half* X, int M, const uint32_t* qweight, const __hal
                     cudaStream_t st) {
   return launch_gemv_mma_plan(plan_gemv_mma(M, N, K, sm_count()), X, M, qweight, scales, zeros,
                               inv_s, N, K, Y, st);
+}
+
+int set_gemv_stall(int withhold, uint64_t wait_ns) {
+  const unsigned w = withhold ? 1u : 0u;
+  const unsigned long long ns = wait_ns;
+  AWQ_CUDA_TRY(cudaMemcpyToSymbol(g_gemv_withhold, &w, sizeof(w)));
+  AWQ_CUDA_TRY(cudaMemcpyToSymbol(g_gemv_wait_ns, &ns, sizeof(ns)));
+  return AWQ_OK;
 }
 
 int read_clear_gemv_error(cudaStream_t st, unsigned* flags) {

@@ -71,6 +71,8 @@ int launch_gemv_mma(const __half* X, int M, const uint32_t* qweight, const __hal
                     const uint32_t* zeros, const float* inv_s, int N, int K, __half* Y,
                     cudaStream_t st);
 int read_clear_gemv_error(cudaStream_t st, unsigned* flags);
+// Test hook of the decode matmul's bounded waits (device-wide, current device).
+int set_gemv_stall(int withhold, uint64_t wait_ns);
 
 // awq_measure.cu: streaming read of `bytes` (a multiple of 16) for the
 // bandwidth ceiling of a chain of launches; `out` receives nothing unless the
@@ -114,6 +116,8 @@ GemmPlan plan_gemm(int M, int N, int K, int mode);
 size_t gemm_partial_bytes(int M, int N, int K);   // split-K workspace of the plain matmul
 int gemm_sqerr_slots(int M);   // number of partial rows kGemmSqErr writes
 int read_clear_gemm_error(cudaStream_t st, unsigned* flags);
+// Test hook of the wide tensor-core matmul's bounded waits (current device).
+int set_gemm_stall(int withhold, uint64_t wait_ns);
 // Y[m][n] = fp16(sum over s < splits of part[s][m][n]), part fp32 [splits][M][N].
 int launch_splitk_reduce(const float* part, int splits, int M, int N, __half* Y,
                          cudaStream_t st);
