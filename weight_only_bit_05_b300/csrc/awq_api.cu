@@ -196,6 +196,7 @@ size_t awq_absmean_workspace_size(int64_t T, int32_t K) {
 
 int awq_absmean(const uint16_t* X, int64_t T, int32_t K, float* a, void* workspace,
                 size_t ws_bytes, void* stream) {
+  NvtxRange range("awq_absmean");
   if (T <= 0 || K <= 0 || K % kGroup != 0) {
     set_error("awq_absmean: T = %lld must be >= 1 and K = %d a positive multiple of 128",
               (long long)T, K);
@@ -214,6 +215,7 @@ int awq_absmean(const uint16_t* X, int64_t T, int32_t K, float* a, void* workspa
 
 int awq_channel_scales(const float* a, int32_t K, double alpha, float* s_c, float* inv_s,
                        void* stream) {
+  NvtxRange range("awq_channel_scales");
   if (K <= 0 || K % kGroup != 0) {
     set_error("awq_channel_scales: K = %d must be a positive multiple of 128", K);
     return AWQ_ERR_SHAPE;
@@ -230,6 +232,7 @@ int awq_channel_scales(const float* a, int32_t K, double alpha, float* s_c, floa
 
 int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K, const awq_config* cfg,
              uint32_t* qweight, uint16_t* scales, uint32_t* zeros, void* stream) {
+  NvtxRange range("awq_pack");
   AWQ_TRY(check_cfg(cfg));
   AWQ_TRY(check_kn(N, K));
   AWQ_TRY(check_ptr(W, "W"));
@@ -247,6 +250,7 @@ int awq_pack(const uint16_t* W, const float* s_c, int32_t N, int32_t K, const aw
 int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M, const uint32_t* qweight,
                 const uint16_t* scales, const uint32_t* zeros, const float* inv_s, int32_t N,
                 int32_t K, uint16_t* Y, void* stream) {
+  NvtxRange range("awq_gemv_ex");
   AWQ_TRY(check_cfg(cfg));
   const awq_config c = cfg ? *cfg : awq_default_config();
   AWQ_TRY(check_kn(N, K));
@@ -275,6 +279,7 @@ int awq_gemv(const uint16_t* X, int32_t M, const uint32_t* qweight, const uint16
 int awq_gemv_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
                       const uint16_t* scales, const uint32_t* zeros, const float* inv_s,
                       int32_t I, int32_t K, uint16_t* Y, void* stream) {
+  NvtxRange range("awq_gemv_silu_mul");
   if (I <= 0 || I % 4 != 0) {
     set_error("awq_gemv_silu_mul: I = %d must be a positive multiple of 4", I);
     return AWQ_ERR_SHAPE;
@@ -297,6 +302,7 @@ int awq_gemv_silu_mul(const uint16_t* X, int32_t M, const uint32_t* qweight,
 
 int awq_fold_inv_scales(const uint16_t* W, int64_t rows, int64_t cols, const float* inv_s,
                         uint16_t* out, void* stream) {
+  NvtxRange range("awq_fold_inv_scales");
   if (rows < 1 || cols < 1) {
     set_error("awq_fold_inv_scales: rows = %lld and cols = %lld must be >= 1",
               static_cast<long long>(rows), static_cast<long long>(cols));
@@ -327,6 +333,7 @@ int awq_clip_search(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32_t
                     const float* s_c, const float* inv_s, const awq_config* cfg, int32_t n_clip,
                     void* workspace, size_t ws_bytes, uint8_t* clip_idx, float* err_out,
                     void* stream) {
+  NvtxRange range("awq_clip_search");
   AWQ_TRY(check_cfg(cfg));
   const awq_config c = cfg ? *cfg : awq_default_config();
   AWQ_TRY(check_kn(N, K));
@@ -359,6 +366,7 @@ int awq_clip_search(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32_t
 int awq_pack_clipped(const uint16_t* W, const float* s_c, int32_t N, int32_t K,
                      const awq_config* cfg, const uint8_t* clip_idx, int32_t n_clip,
                      uint32_t* qweight, uint16_t* scales, uint32_t* zeros, void* stream) {
+  NvtxRange range("awq_pack_clipped");
   AWQ_TRY(check_cfg(cfg));
   AWQ_TRY(check_kn(N, K));
   if (n_clip < 1 || n_clip > 200) {
@@ -389,6 +397,7 @@ int gemm_common(int mode, const awq_config* cfg, const uint16_t* X, int32_t M,
                 const uint32_t* qweight, const uint16_t* scales, const uint32_t* zeros,
                 const float* inv_s, int32_t N, int32_t K, uint16_t* Y, int32_t ldy,
                 void* workspace, size_t ws_bytes, void* stream) {
+  NvtxRange range(mode == kGemmSiluF16 ? "awq_gemm_silu_mul" : "awq_gemm");
   AWQ_TRY(check_cfg(cfg));
   const awq_config c = cfg ? *cfg : awq_default_config();
   AWQ_TRY(check_kn(N, K));
@@ -470,6 +479,7 @@ int awq_debug_stall(int32_t which, int64_t wait_limit_ns) {
 
 int awq_measure_stream_read(const void* buf, size_t bytes, int32_t read_first, uint32_t* out,
                             void* stream) {
+  NvtxRange range("awq_measure_stream_read");
   if (bytes == 0 || bytes % 16 != 0) {
     set_error("awq_measure_stream_read: bytes = %zu must be a positive multiple of 16", bytes);
     return AWQ_ERR_SHAPE;

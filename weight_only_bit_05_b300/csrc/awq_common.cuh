@@ -11,6 +11,8 @@
 #include <cstdio>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/awq.h"
 
 namespace awq {
@@ -30,6 +32,16 @@ int cuda_status(cudaError_t e, const char* what);
     cudaError_t _e = (call);                                 \
     if (_e != cudaSuccess) return ::awq::cuda_status(_e, #call); \
   } while (0)
+
+// An NVTX range named after a C-ABI entry point for the duration of the call,
+// so that a profiler attributes the call's launches to it (header-only NVTX:
+// a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

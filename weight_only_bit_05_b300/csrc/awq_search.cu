@@ -107,6 +107,7 @@ int awq_search_scales(const uint16_t* X_cal, int64_t T, const uint16_t* W, int32
                       const awq_config* cfg, void* workspace, size_t ws_bytes, float* s_c_out,
                       float* inv_s_out, int32_t* best_out, double* mse_out, double* row_err_out,
                       void* stream) {
+  NvtxRange range("awq_search_scales");
   const awq_config c = cfg ? *cfg : awq_default_config();
   if ((c.w_bit != 4 && c.w_bit != 8) || (c.group != 128 && c.group != 64 && c.group != 32) ||
       (c.zero_point != 0 && c.zero_point != 1) || c.n_grid < 1 || c.n_grid > 64) {
