@@ -179,7 +179,10 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
                 const float* inv_s, int32_t N, int32_t K, uint16_t* Y, void* stream);
 
 /* ------------------------------------------------------------- GEMM, any M
- * Same result as awq_gemv for any M >= 1, on the 5th-generation tensor cores:
+ * Same result as awq_gemv for any M >= 1. For M <= 8 with the default format
+ * (K % 256 == 0) it runs awq_gemv's decode matmul whenever that needs no K
+ * split (the workspace is then unused). Otherwise on the 5th-generation
+ * tensor cores:
  * packed codes and activations staged by TMA, codes dequantized to fp16 in
  * shared memory, tcgen05.mma (fp16 x fp16, fp32 accumulation in tensor
  * memory). For M <= 128 with 4- or 8-bit codes in 128- or 64-channel groups

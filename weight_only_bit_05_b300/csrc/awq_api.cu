@@ -412,6 +412,21 @@ int gemm_common(int mode, const awq_config* cfg, const uint16_t* X, int32_t M,
   AWQ_TRY(check_opt_ptr(inv_s, "inv_s"));
   AWQ_TRY(check_ptr(Y, "Y"));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (inv_s && (!workspace || !aligned16(workspace) || ws_bytes < xt_bytes(M, K))) {
+    set_error("awq_gemm: workspace must be 16-B aligned and >= %zu bytes",
+              awq_gemm_workspace_size(M, N, K));
+    return AWQ_ERR_WORKSPACE;
+  }
+  // up to 8 tokens of the default format: the decode matmul (warp-level MMA,
+  // weights streamed by TMA) when it runs without a K split; it scales the
+  // activations itself, so the workspace is not used
+  if (mode == kGemmOutF16 && gemv_mma_eligible(M, K, c.w_bit, c.group, false)) {
+    const MmaGemvPlan p = plan_gemv_mma(M, N, K, sm_count());
+    if (p.depth > 0 && p.nsplit == 1)
+      return launch_gemv_mma_plan(p, reinterpret_cast<const __half*>(X), M, qweight,
+                                  reinterpret_cast<const __half*>(scales), zeros, inv_s, N, K,
+                                  reinterpret_cast<__half*>(Y), st);
+  }
   const __half* xt = reinterpret_cast<const __half*>(X);
   // workspace: X~ first (when inv_s is given), then the split-K partial sums
   // if the rest of the workspace holds them

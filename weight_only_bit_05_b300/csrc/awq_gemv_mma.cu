@@ -520,13 +520,18 @@ MmaGemvPlan make_gemv_mma_plan(int M, int N, int K, int sms, int warps, int ctas
   return p;
 }
 
-// The launch plan the library uses: two CTAs of eight warps per SM, each
-// warp with a ring of two 4 KB stages (measured fastest on the Llama-2
-// decode shapes, against deeper rings, one CTA of 8 or 16 warps per SM, and
-// one CTA beside the next launch's); one CTA per SM when the activations do
-// not fit half an SM.
+// The launch plan the library uses, in order of preference (measured on the
+// Llama-2 decode shapes): two CTAs of eight warps per SM, each warp with a
+// ring of two 4 KB stages (fastest at M = 1, against deeper rings, one CTA of
+// 8, 12 or 16 warps per SM, and one CTA beside the next launch's); when the
+// activations of several tokens do not fit half an SM, one CTA of sixteen
+// warps per SM (the activations once per SM); a K split over a cluster only
+// when neither fits.
 MmaGemvPlan plan_gemv_mma(int M, int N, int K, int sms) {
   MmaGemvPlan p = make_gemv_mma_plan(M, N, K, sms, 8, 2, 2, 2);
+  if (p.depth > 0 && p.nsplit == 1) return p;
+  const MmaGemvPlan q = make_gemv_mma_plan(M, N, K, sms, 16, 1, 2, 2);
+  if (q.depth > 0 && q.nsplit == 1) return q;
   if (p.depth == 0) p = make_gemv_mma_plan(M, N, K, sms, 8, 1, 2, kMaxDepth);
   return p;
 }
