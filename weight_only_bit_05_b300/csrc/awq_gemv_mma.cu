@@ -173,8 +173,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   const int klen = min(K - kbeg, KS);
   const int C = (klen + kStageK - 1) / kStageK;          // stages per tile
   const int S = T * C;
-  const int sb = static_cast<int>(static_cast<int64_t>(warp) * S / kWarps);
-  const int se = static_cast<int>(static_cast<int64_t>(warp + 1) * S / kWarps);
+  const int sb = warp * S / kWarps, se = (warp + 1) * S / kWarps;   // S * kWarps < 2^31
   const int xstride = (KS / 128) * 256 + 64;             // bytes per token row of x~
 
   // first physical row of tile t: the last tile ends at r1 (may start below r0)
@@ -260,35 +259,54 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // (8 channels k = 128 gl + 32 cc + 8 jj + i) sits at gl * 256 + jj * 64 +
   // cc * 16 and holds the pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) that the
   // dequantization produces
-  const int nv = klen / 8;
-  for (int q = threadIdx.x; q < M * nv; q += kThreads) {
-    const int m = q / nv, v = q - m * nv;
-    const int k = kbeg + 8 * v;
-    const uint4 xr = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + k));
-    const __half2* xh = reinterpret_cast<const __half2*>(&xr);
-    float f[8];
+  // Up to kBatch vectors per thread have their loads in flight together
+  // (the loads wait behind the weight stream in L2: one latency per batch)
+  const int nv = klen / 8, nitems = M * nv;
+  constexpr int kBatch = 4;
+  for (int base = threadIdx.x; base < nitems; base += kThreads * kBatch) {
+    uint4 xr[kBatch];
+    float4 ia[kBatch], ib[kBatch];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 t2 = __half22float2(xh[i]);
-      f[2 * i] = t2.x;
-      f[2 * i + 1] = t2.y;
+    for (int u = 0; u < kBatch; ++u) {
+      const int q = base + u * kThreads;
+      if (q < nitems) {
+        const int m = q / nv, v = q - m * nv;
+        const int k = kbeg + 8 * v;
+        xr[u] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + k));
+        if (inv_s) {
+          ia[u] = __ldg(reinterpret_cast<const float4*>(inv_s + k));
+          ib[u] = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
+        }
+      }
     }
-    if (inv_s) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
-      const float is[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], is[i]);
-    }
-    uint4 o;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+    for (int u = 0; u < kBatch; ++u) {
+      const int q = base + u * kThreads;
+      if (q >= nitems) break;
+      const int m = q / nv, v = q - m * nv;
+      const __half2* xh = reinterpret_cast<const __half2*>(&xr[u]);
+      float f[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 p2 = __halves2half2(__float2half_rn(f[i]), __float2half_rn(f[i + 4]));
-      ow[i] = *reinterpret_cast<const uint32_t*>(&p2);
+      for (int i = 0; i < 4; ++i) {
+        const float2 t2 = __half22float2(xh[i]);
+        f[2 * i] = t2.x;
+        f[2 * i + 1] = t2.y;
+      }
+      if (inv_s) {
+        const float is[8] = {ia[u].x, ia[u].y, ia[u].z, ia[u].w, ib[u].x, ib[u].y, ib[u].z, ib[u].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], is[i]);
+      }
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 p2 = __halves2half2(__float2half_rn(f[i]), __float2half_rn(f[i + 4]));
+        ow[i] = *reinterpret_cast<const uint32_t*>(&p2);
+      }
+      const int gl = v >> 4, cc = (v >> 2) & 3, jj = v & 3;
+      *reinterpret_cast<uint4*>(xsb + m * xstride + gl * 256 + jj * 64 + cc * 16) = o;
     }
-    const int gl = v >> 4, cc = (v >> 2) & 3, jj = v & 3;
-    *reinterpret_cast<uint4*>(xsb + m * xstride + gl * 256 + jj * 64 + cc * 16) = o;
   }
   __syncthreads();
 
@@ -444,8 +462,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
     int nw = 0;
     bool whole = false;
     for (int w = 0; w < kWarps; ++w) {
-      const int wb = static_cast<int>(static_cast<int64_t>(w) * S / kWarps);
-      const int we = static_cast<int>(static_cast<int64_t>(w + 1) * S / kWarps);
+      const int wb = w * S / kWarps, we = (w + 1) * S / kWarps;   // S * kWarps < 2^31
       if (we <= s0 || wb >= s1 || wb == we) continue;
       if (wb <= s0 && we >= s1) {
         whole = true;
