@@ -790,6 +790,8 @@ def main():
                     help="skip the quantization-variant figures")
     ap.add_argument("--only-gemm", default=None, metavar="MODEL:LAYER:M",
                     help="run only awq_gemm on one shape 3 times (a small case for profilers)")
+    ap.add_argument("--only-gemv", default=None, metavar="MODEL:LAYER:M",
+                    help="run only awq_gemv on one shape 3 times (a small case for profilers)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -828,6 +830,19 @@ def main():
     import torch
     import weight_only_bit_05_b300 as awq
     torch.cuda.set_device(local)
+    if args.only_gemv:
+        model, name, M = args.only_gemv.split(":")
+        K, N, lid = awq_inputs.layer(model, name)
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(1000 + lid)
+        qw, sc, zs = awq.pack((torch.randn((N, K), generator=gen, device="cuda") * 0.02).half())
+        X = torch.randn((int(M), K), generator=gen, device="cuda").half()
+        inv_s = torch.rand(K, generator=gen, device="cuda") + 0.5
+        for _ in range(3):
+            awq.gemv(X, qw, sc, zs, inv_s)
+        awq.check_device_error()
+        print("ok", args.only_gemv)
+        return
     if args.only_gemm:
         model, name, M = args.only_gemm.split(":")
         K, N, lid = awq_inputs.layer(model, name)
