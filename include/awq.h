@@ -194,9 +194,12 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
  * X~ = fp16(X * inv_s) is first written
  * to the workspace; with inv_s == NULL X is read directly and the workspace
  * may be NULL. awq_gemm_workspace_size also counts the fp32 partial sums of a
- * split-K launch (chosen when the layer has too few 128-row tiles to fill the
- * GPU; the splits are added in a fixed order by a second kernel): a smaller
- * workspace, at least X~ when inv_s is given, runs without split-K.
+ * split-K launch, chosen either when the layer has too few 128-row tiles to
+ * fill the GPU (every tile split over K) or when the tiles fill a few rounds
+ * of the SMs and leave a ragged last one (only that round's tiles split, so
+ * their parts occupy the SMs that would idle); a second kernel adds each
+ * tile's parts in a fixed order. A smaller workspace, at least X~ when inv_s
+ * is given, runs without split-K.
  * Y: fp16 [M][N]. */
 AWQ_API size_t awq_gemm_workspace_size(int32_t M, int32_t N, int32_t K);
 AWQ_API int awq_gemm(const uint16_t* X, int32_t M, const uint32_t* qweight,

@@ -33,11 +33,15 @@ def test_default_config_and_workspace_sizes():
     assert (c.w_bit, c.group, c.zero_point, c.n_grid) == (4, 128, 1, 20)
     assert lib.awq_gemm_workspace_size(16, 512, 512) == 16 * 512 * 2
     # few 128-row tiles: the plans split K, and the workspace also holds the
-    # fp32 partial sums (narrow-token kernel up to 128 tokens, wide above)
-    for M, N, K in ((16, 256, 4096), (120, 256, 4096), (48, 640, 8192), (300, 1024, 8192)):
+    # fp32 partial sums, at most 8 parts of [M][N] for the narrow-token kernel
+    # (up to 128 tokens) or of each [bn][128] tile (bn = the token tile) for
+    # the wide one
+    for M, N, K, bn in ((16, 256, 4096, 16), (120, 256, 4096, 128), (48, 640, 8192, 64),
+                        (300, 1024, 8192, 256)):
         xt = ((M * K * 2 + 255) // 256) * 256
         part = lib.awq_gemm_workspace_size(M, N, K) - xt
-        assert part > 0 and part % (M * N * 4) == 0 and part // (M * N * 4) <= 8, (M, N, K)
+        padded = -(-M // bn) * bn * -(-N // 128) * 128 * 4
+        assert part > 0 and part % 4 == 0 and part <= 8 * max(padded, M * N * 4), (M, N, K)
     assert lib.awq_gemm_workspace_size(0, 512, 512) == 0
     assert lib.awq_absmean_workspace_size(4096, 4096) % 8 == 0
     assert lib.awq_absmean_workspace_size(4096, 4096) >= 4096 * 8

@@ -64,3 +64,31 @@ def test_splitk_variants(w_bit, group):
     y_ref, base = O.linear(X16, qw, sc, zs, inv_s, group, w_bit)
     err = np.abs(y.astype(np.float64) - y_ref)
     assert np.all(err <= O.tolerance(y_ref, base))
+
+
+def _tiles(M, N):
+    bn = 256 if M > 128 else max(16, 1 << (M - 1).bit_length())
+    return -(-N // 128) * -(-M // bn)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 9736, 4096), (2048, 5120, 5120), (2048, 5120, 13824)])
+def test_ragged_round_split(M, N, K):
+    """More tiles than SMs with a ragged last round: only that round's tiles
+    are split over K.  (300, 9736): the split tiles are the ragged last token
+    tile and include the ragged last row tile; the other two are the 13B o and
+    down layers at 2048 tokens.  Every output of the split tiles (the last
+    token tile) and a sample of the other tokens are checked; repeated calls
+    are bitwise equal."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = _tiles(M, N)
+    assert tiles > sms and tiles % sms != 0
+    assert _split_bytes(M, N, K) > 0, "the plan is expected to split the last round"
+    rng, qw, sc, zs, inv_s = _layer(M + N + K, N, K)
+    X16 = rng.standard_normal((M, K)).astype(np.float16)
+    args = (dev(X16), dev(qw), dev(sc), dev(zs), dev(inv_s))
+    y1 = host(awq.gemm(*args))
+    y2 = host(awq.gemm(*args))
+    assert np.array_equal(y1.view(np.uint16), y2.view(np.uint16))
+    last = np.arange(((M - 1) // 256) * 256, M)
+    sample = np.unique(np.concatenate([last, np.arange(0, M, 61)]))
+    assert_linear_close(y1, X16, qw, sc, zs, inv_s, cols=sample)

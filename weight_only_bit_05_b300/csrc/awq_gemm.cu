@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_a,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros, int M,
                 int N, int K, int gs, void* __restrict__ out, int ldo,
-                const float* __restrict__ yref, int ldy, int splits, int kps,
+                const float* __restrict__ yref, int ldy, int full_tiles, int ts, int kps,
                 float* __restrict__ part) {
   using C = Cfg<BN, MODE, BITS>;
   constexpr int KWB = BK * BITS / 32;   // packed words of one row per stage
@@ -197,15 +197,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = K / BK;
   const int n_tiles = (N + BM - 1) / BM;
   const int tiles = n_tiles * ((M + BN - 1) / BN);
-  // split-K: work item t is tile t / splits over the k-blocks [kb0, kb1) of
-  // split t % splits, kps of them (an even number, so that no split starts
-  // inside a 128-channel group; the host guarantees every split is
-  // non-empty); with splits > 1 the epilogue writes fp32 partial sums to
-  // part[split][M][ldo] and a second kernel adds them
-  const int items = tiles * splits;
-  auto krange = [&](int t, int& kb0, int& kb1) {
-    kb0 = (t % splits) * kps;
-    kb1 = kb0 + kps < nk ? kb0 + kps : nk;
+  // Work items: items t < full_tiles are the whole tiles 0 .. full_tiles - 1
+  // (fp16 output); the remaining tiles are split over K, ts ways each: item
+  // full_tiles + u is part u % ts of tile full_tiles + u / ts, k-blocks
+  // [kb0, kb1), kps of them (an even number, so that no part starts inside
+  // a 128-channel group; the host guarantees every part is non-empty).  A
+  // part writes fp32 partial sums to its own [BN][BM] block of `part` and a
+  // second kernel adds a tile's parts in order.  Plain split-K over every
+  // tile is full_tiles = 0; no split at all is ts = 1.
+  const int items = full_tiles + (tiles - full_tiles) * ts;
+  auto item_of = [&](int t, int& tile, int& kb0, int& kb1, int& split) {
+    if (t < full_tiles) {
+      tile = t;
+      split = -1;
+      kb0 = 0;
+      kb1 = nk;
+      return;
+    }
+    const int u = t - full_tiles, q = u / ts;
+    tile = full_tiles + q;
+    split = ts > 1 ? u - q * ts : -1;
+    kb0 = ts > 1 ? (u - q * ts) * kps : 0;
+    kb1 = ts > 1 && kb0 + kps < nk ? kb0 + kps : nk;
   };
 
   if (threadIdx.x == 0) {
@@ -245,10 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // test hook: the first stage of the first CTA is never requested
       const bool withhold = g_gemm_withhold != 0 && blockIdx.x == 0;
       for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
-        const int tile = t / splits;
+        int tile, kb0, kb1, split;
+        item_of(t, tile, kb0, kb1, split);
         const int n0 = (tile % n_tiles) * BM, m0 = (tile / n_tiles) * BN;
-        int kb0, kb1;
-        krange(t, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
           if (it >= S && !wait_or_abort(empty + s, ((it / S) - 1) & 1, ab, 1u)) {
@@ -294,8 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lt >= 2 && !wait_or_abort(acc_empty + b, ((lt >> 1) - 1) & 1, ab, 2u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * C::ACC_COLS;
-        int kb0, kb1;
-        krange(t, kb0, kb1);
+        int tile, kb0, kb1, split;
+        item_of(t, tile, kb0, kb1, split);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -345,9 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
         // with the fused gate/up weight, MMA row r of the tile is virtual row
         // v = n0 + r: gate row v/2 for even v, up row v/2 for odd v
-        const int v = ((t / splits) % n_tiles) * BM + r;
-        int kb0, kb1;
-        krange(t, kb0, kb1);
+        int tile, kb0, kb1, split;
+        item_of(t, tile, kb0, kb1, split);
+        const int v = (tile % n_tiles) * BM + r;
         const int n = MODE == kGemmSiluF16 ? (v >> 1) + (v & 1) * (N / 2) : v;
         const bool row_ok = MODE == kGemmSiluF16 ? (v >> 1) < N / 2 : v < N;
         const int raw_r = MODE == kGemmSiluF16 ? (r >> 1) + (r & 1) * (BM / 2) : r;
@@ -459,9 +471,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     int lt = 0;
     for (int t = blockIdx.x; t < items; t += gridDim.x, ++lt) {
-      const int tile = t / splits;
+      int tile, kb0, kb1, split;
+      item_of(t, tile, kb0, kb1, split);
       const int n0 = (tile % n_tiles) * BM, mt = tile / n_tiles, m0 = mt * BN;
-      float* pout = part + static_cast<size_t>(t % splits) * M * ldo;   // splits > 1
+      // a split tile's [BN][BM] block of partial sums for this part
+      float* pout = split >= 0 ? part + (static_cast<size_t>(tile - full_tiles) * ts + split) *
+                                            BN * BM
+                               : nullptr;
       const int b = lt & 1;
       const int n = n0 + quarter * 32 + lane;
       if (!wait_or_abort(acc_full + b, (lt >> 1) & 1, ab, 8u)) break;
@@ -495,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float val = __uint_as_float(v[j]);
               const size_t idx = static_cast<size_t>(m) * ldo + n;
               if (MODE == kGemmOutF16) {
-                if (splits > 1)
-                  pout[idx] = val;
+                if (split >= 0)
+                  pout[(m - m0) * BM + (n - n0)] = val;
                 else
                   static_cast<__half*>(out)[idx] = __float2half_rn(val);
               } else if (MODE == kGemmDenseF32) {
@@ -553,6 +569,58 @@ __global__ void prescale_kernel(const __half* __restrict__ X, const float* __res
   reinterpret_cast<uint4*>(Xt)[i] = o;
 }
 
+// The split tiles of the wide kernel: Y[m][n] = fp16(sum over s of the
+// tile's part blocks, in order).  Tile full_tiles + tt, part s is the
+// [bn][BM] block (tt * ts + s) of `part`.
+__global__ void tile_reduce_kernel(const float* __restrict__ part, int full_tiles,
+                                   int tail_tiles, int ts, int n_tiles, int bn, int M, int N,
+                                   __half* __restrict__ Y, int ldo) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  constexpr int Q = BM / 4;   // float4 per block row
+  const int64_t blk4 = static_cast<int64_t>(bn) * Q;   // float4 per [bn][BM] block
+  const int64_t total = static_cast<int64_t>(tail_tiles) * blk4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int tt = static_cast<int>(i / blk4);
+    const int rem = static_cast<int>(i - tt * blk4);
+    const int ml = rem / Q, n4 = rem - ml * Q;
+    const int tile = full_tiles + tt;
+    const int m = (tile / n_tiles) * bn + ml, n = (tile % n_tiles) * BM + 4 * n4;
+    if (m >= M || n >= N) continue;
+    const float4* src = reinterpret_cast<const float4*>(part) + tt * ts * blk4 + rem;
+    float4 a = src[0];
+    for (int s2 = 1; s2 < ts; ++s2) {
+      const float4 b = src[s2 * blk4];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    __half2* y = reinterpret_cast<__half2*>(Y + static_cast<size_t>(m) * ldo + n);
+    y[0] = __floats2half2_rn(a.x, a.y);
+    y[1] = __floats2half2_rn(a.z, a.w);
+  }
+}
+
+int launch_tile_reduce(const float* part, int full_tiles, int tail_tiles, int ts, int n_tiles,
+                       int bn, int M, int N, __half* Y, int ldo, cudaStream_t st) {
+  const int64_t total = static_cast<int64_t>(tail_tiles) * bn * (BM / 4);
+  const int64_t want = (total + 255) / 256, cap = static_cast<int64_t>(sm_count()) * 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, tile_reduce_kernel, part, full_tiles, tail_tiles, ts,
+                                  n_tiles, bn, M, N, Y, ldo));
+  return AWQ_OK;
+}
+
 // Y[m][n] = fp16(sum over s of part[s][m][n]), the splits added in order.
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t mn4,
                                      __half* __restrict__ Y) {
@@ -576,8 +644,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 template <int BN, int MODE, bool PERM, int BITS>
 int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
                 const uint32_t* zeros, int M, int N, int K, int gs, void* out, int ldo,
-                const float* yref, int ldy, cudaStream_t st, int splits = 1, int kps = 0,
-                float* part = nullptr) {
+                const float* yref, int ldy, cudaStream_t st, int full_tiles = 0, int ts = 1,
+                int kps = 0, float* part = nullptr) {
   using C = Cfg<BN, MODE, BITS>;
   if (kps == 0) kps = K / BK;
   {
@@ -587,7 +655,9 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   }
   cudaLaunchConfig_t cfg = {};
   const int sms = sm_count();
-  const int items = ((N + BM - 1) / BM) * ((M + BN - 1) / BN) * splits;
+  const int n_tiles = (N + BM - 1) / BM;
+  const int tiles = n_tiles * ((M + BN - 1) / BN);
+  const int items = full_tiles + (tiles - full_tiles) * ts;
   cfg.gridDim = dim3(items < sms ? items : sms, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
@@ -598,32 +668,34 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   AWQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE, PERM, BITS>, tb, ta, scales, zeros,
-                                  M, N, K, gs, out, ldo, yref, ldy, splits, kps, part));
-  // ldo == N for the split-K plan: the partials and Y are dense [M][N]
-  if (splits > 1) return launch_splitk_reduce(part, splits, M, N, static_cast<__half*>(out), st);
+                                  M, N, K, gs, out, ldo, yref, ldy, full_tiles, ts, kps, part));
+  if (ts > 1)
+    return launch_tile_reduce(part, full_tiles, tiles - full_tiles, ts, n_tiles, BN, M, N,
+                              static_cast<__half*>(out), ldo, st);
   return AWQ_OK;
 }
 
 template <int MODE, bool PERM, int BITS>
 int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __half* scales,
                 const uint32_t* zeros, int M, int N, int K, int gs, void* out, int ldo,
-                const float* yref, int ldy, cudaStream_t st, int splits, int kps, float* part) {
+                const float* yref, int ldy, cudaStream_t st, int full_tiles, int ts, int kps,
+                float* part) {
   switch (bn) {
     case 16:
       return launch_tile<16, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
-                                               ldy, st, splits, kps, part);
+                                               ldy, st, full_tiles, ts, kps, part);
     case 32:
       return launch_tile<32, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
-                                               ldy, st, splits, kps, part);
+                                               ldy, st, full_tiles, ts, kps, part);
     case 64:
       return launch_tile<64, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo, yref,
-                                               ldy, st, splits, kps, part);
+                                               ldy, st, full_tiles, ts, kps, part);
     case 128:
       return launch_tile<128, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
-                                                yref, ldy, st, splits, kps, part);
+                                                yref, ldy, st, full_tiles, ts, kps, part);
     default:
       return launch_tile<256, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
-                                                yref, ldy, st, splits, kps, part);
+                                                yref, ldy, st, full_tiles, ts, kps, part);
   }
 }
 
@@ -639,48 +711,65 @@ int pick_bn(int M, int mode) {
 }  // namespace
 
 // Token-tile width and split-K for one launch.  The tile is the smallest of
-// 16..256 tokens that holds M; split-K comes from a cost model in SM cycles:
-// a k-block of a work item costs max(2 BN, 208) cycles (tensor-core work of a
-// 128 x BN x 64 MMA, or the 8 dequantization warps' share of 1024 packed
-// words, whichever is larger); items run in rounds of one per SM; a split-K
-// plan pays the fp32 partial sums written and read back (8 bytes per output
-// per split at ~3250 bytes per cycle) and a second launch.  Only the plain
-// fp16 output takes split-K (at most 8 splits of >= 8 k-blocks each).
+// 16..256 tokens that holds M; the split comes from a cost model in SM
+// cycles: a k-block of a work item costs max(2 BN, 208) cycles (tensor-core
+// work of a 128 x BN x 64 MMA, or the 8 dequantization warps' share of 1024
+// packed words, whichever is larger); items run in rounds of one per SM; a
+// split pays its fp32 partial sums written and read back (8 bytes per output
+// per part at ~3250 bytes per cycle) and a second launch.  Two kinds of split
+// are weighed against none: every tile split s ways (for fewer tiles than
+// SMs), and only the last, partial round of tiles split so that its parts
+// fill the SMs that would otherwise idle while the other SMs run their
+// whole tiles (for a few full rounds and a ragged one).  Only the plain fp16
+// output splits (at most 8 parts of >= 8 k-blocks each).
 GemmPlan plan_gemm(int M, int N, int K, int mode) {
   const int sms = sm_count();
   const int nk = K / BK;
   const int n_tiles = (N + BM - 1) / BM;
-  GemmPlan best{pick_bn(M, mode), 1, nk};
-  double best_t = -1.0;
-  {
-    // above 128 tokens the widest tile (measured: 128-token tiles lose more
-    // to per-stage overheads than they win back on wave quantization)
-    const int bn = pick_bn(M, mode);
-    const int tiles = n_tiles * ((M + bn - 1) / bn);
-    const double c = 2.0 * bn > 208.0 ? 2.0 * bn : 208.0;
-    const int max_s = mode == kGemmOutF16 ? 8 : 1;
-    for (int s = 1; s <= max_s; ++s) {
-      const int kps = ((nk + s - 1) / s + 1) & ~1;
-      if (s > 1 && kps < 8) break;
-      const int s_eff = (nk + kps - 1) / kps;
-      if (s_eff != s) continue;
-      const int items = tiles * s;
-      const int rounds = (items + sms - 1) / sms;
-      double t = static_cast<double>(rounds) * kps * c;
-      if (s > 1) t += 8.0 * s * static_cast<double>(M) * N / 3250.0 + 2000.0;
-      if (best_t < 0 || t < best_t) {
+  // above 128 tokens the widest tile (measured: 128-token tiles lose more to
+  // per-stage overheads than they win back on wave quantization)
+  const int bn = pick_bn(M, mode);
+  const int tiles = n_tiles * ((M + bn - 1) / bn);
+  const double c = 2.0 * bn > 208.0 ? 2.0 * bn : 208.0;
+  const double part_cost = 8.0 * bn * BM / 3250.0;   // per split tile and part
+  GemmPlan best{bn, 0, 1, nk};
+  double best_t = static_cast<double>((tiles + sms - 1) / sms) * nk * c;
+  if (mode != kGemmOutF16) return best;
+  const int rounds_full = tiles / sms, tail = tiles - rounds_full * sms;
+  for (int s = 2; s <= 8; ++s) {
+    const int kps = ((nk + s - 1) / s + 1) & ~1;
+    if (kps < 8) break;
+    if ((nk + kps - 1) / kps != s) continue;
+    // every tile split
+    {
+      const int rounds = (tiles * s + sms - 1) / sms;
+      const double t = static_cast<double>(rounds) * kps * c + part_cost * tiles * s + 2000.0;
+      if (t < best_t) {
         best_t = t;
-        best = GemmPlan{bn, s, kps};
+        best = GemmPlan{bn, 0, s, kps};
+      }
+    }
+    // the ragged last round split, one part per otherwise idle SM
+    if (rounds_full >= 1 && tail > 0 && tail * s <= sms) {
+      const double t = (static_cast<double>(rounds_full) * nk + kps) * c + part_cost * tail * s +
+                       2000.0;
+      if (t < best_t) {
+        best_t = t;
+        best = GemmPlan{bn, rounds_full * sms, s, kps};
       }
     }
   }
-  if (best.splits == 1) best.kps = nk;
   return best;
 }
 
+static size_t gemm_split_bytes(const GemmPlan& p, int M, int N) {
+  if (p.ts <= 1) return 0;
+  const int tiles = ((N + BM - 1) / BM) * ((M + p.bn - 1) / p.bn);
+  return static_cast<size_t>(tiles - p.full_tiles) * p.ts * p.bn * BM * sizeof(float);
+}
+
 size_t gemm_partial_bytes(int M, int N, int K) {
-  const GemmPlan p = plan_gemm(M, N, K, kGemmOutF16);
-  const size_t wide = p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 0;
+  const size_t wide = gemm_split_bytes(plan_gemm(M, N, K, kGemmOutF16), M, N);
   const size_t narrow = narrow_partial_bytes(M, N, K);
   return wide > narrow ? wide : narrow;
 }
@@ -730,21 +819,22 @@ template <int BITS>
 int launch_gemm_bits(int mode, int bn, const CUtensorMap& tb, const CUtensorMap& ta,
                      bool xt_permuted, int M, const __half* scales, const uint32_t* zeros, int N,
                      int K, int gs, void* out, int ldo, const float* yref, int ldy,
-                     cudaStream_t st, int splits, int kps, float* part) {
+                     cudaStream_t st, int full_tiles, int ts, int kps,
+                     float* part) {
   switch (mode) {
     case kGemmOutF16:
       if (xt_permuted)
         return dispatch_bn<kGemmOutF16, true, BITS>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                    ldo, yref, ldy, st, splits, kps, part);
+                                                    ldo, yref, ldy, st, full_tiles, ts, kps, part);
       return dispatch_bn<kGemmOutF16, false, BITS>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                   ldo, yref, ldy, st, splits, kps, part);
+                                                   ldo, yref, ldy, st, full_tiles, ts, kps, part);
     case kGemmSiluF16:
       if constexpr (BITS == 4) {
         if (xt_permuted)
           return dispatch_bn<kGemmSiluF16, true, 4>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                    ldo, yref, ldy, st, 1, 0, nullptr);
+                                                    ldo, yref, ldy, st, 0, 1, 0, nullptr);
         return dispatch_bn<kGemmSiluF16, false, 4>(bn, tb, ta, scales, zeros, M, N, K, gs, out,
-                                                   ldo, yref, ldy, st, 1, 0, nullptr);
+                                                   ldo, yref, ldy, st, 0, 1, 0, nullptr);
       }
       set_error("the fused gate/up layer takes 4-bit codes");
       return AWQ_ERR_UNSUPPORTED;
@@ -775,11 +865,11 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
     return launch_gemm_narrow(Xt, xt_permuted, M, qweight, scales, zeros, N, K,
                               static_cast<__half*>(out), ldo, st, w_bit, group, part, part_bytes);
   GemmPlan plan = plan_gemm(M, N, K, mode);
-  // split-K needs the partial sums' workspace and a dense [M][N] output
-  if (plan.splits > 1 &&
-      (!part || part_bytes < static_cast<size_t>(plan.splits) * M * N * sizeof(float) ||
-       ldo != N || !aligned16(part))) {
-    plan.splits = 1;
+  // a split needs the partial sums' workspace
+  if (plan.ts > 1 &&
+      (!part || part_bytes < gemm_split_bytes(plan, M, N) || !aligned16(part))) {
+    plan.full_tiles = 0;
+    plan.ts = 1;
     plan.kps = K / BK;
   }
   const int bn = plan.bn;
@@ -803,9 +893,9 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
   if (rc != AWQ_OK) return rc;
   if (w_bit == 8)
     return launch_gemm_bits<8>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
-                               ldo, yref, ldy, st, plan.splits, plan.kps, part);
+                               ldo, yref, ldy, st, plan.full_tiles, plan.ts, plan.kps, part);
   return launch_gemm_bits<4>(mode, bn, tb, ta, xt_permuted, M, scales, zeros, N, K, group, out,
-                             ldo, yref, ldy, st, plan.splits, plan.kps, part);
+                             ldo, yref, ldy, st, plan.full_tiles, plan.ts, plan.kps, part);
 }
 
 int set_gemm_stall(int withhold, uint64_t wait_ns) {

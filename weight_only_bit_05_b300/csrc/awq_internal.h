@@ -108,9 +108,10 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
                 void* out, int ldo, const float* yref, int ldy, cudaStream_t st, int w_bit = 4,
                 int group = 128, float* part = nullptr, size_t part_bytes = 0);
 struct GemmPlan {
-  int bn;       // token-tile width
-  int splits;   // split-K factor
-  int kps;      // k-blocks (64 channels) per split
+  int bn;           // token-tile width
+  int full_tiles;   // tiles 0 .. full_tiles - 1 run whole
+  int ts;           // the rest are split over K, ts ways each (1: no split)
+  int kps;          // k-blocks (64 channels) per split
 };
 GemmPlan plan_gemm(int M, int N, int K, int mode);
 size_t gemm_partial_bytes(int M, int N, int K);   // split-K workspace of the plain matmul
