@@ -45,25 +45,51 @@ namespace {
 
 constexpr int BM = 128;          // weight rows per CTA (MMA M)
 constexpr int BK = 64;           // K per stage: one 128-byte swizzle atom of fp16
-constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * (kDeqWarps + kEpiWarps);
 // limit of the bounded waits, read only on their slow path
 __device__ __forceinline__ uint64_t wait_limit_ns() {
   return *const_cast<volatile unsigned long long*>(&g_gemm_wait_ns);
 }
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
+// At BN = 192 the dequantized operand does not pass through shared memory:
+// the dequantization warps write it into a ring in tensor memory (after the
+// two 192-column accumulators) and the MMA reads A from there.  Shared memory
+// then carries only the activation tile and the packed codes of a stage (and
+// the MMA reads only the activations from it), which keeps its port below
+// the rate at which the MMA consumes stages; with A in shared memory a
+// 256-token stage moves about 104 KB through it, more than the port passes
+// in the 512 cycles of the stage's MMA.
 template <int BN, int MODE, int BITS>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int RAW_ROW = BK * BITS / 8;     // packed bytes of one row per stage
+  static constexpr bool ATM = BN == 192;
+  // 64-channel k-blocks per pipeline stage: two with A in tensor memory, so
+  // that every wait, commit and arrive of the roles serves 8 MMAs, not 4
+  static constexpr int SK = ATM ? 2 : 1;
+  static constexpr int A_BYTES = ATM ? 0 : BM * BK * 2;
+  static constexpr int B_SUB = BN * BK * 2;         // one 64-channel column of activations
+  static constexpr int B_BYTES = B_SUB * SK;
+  static constexpr int RAW_ROW = BK * SK * BITS / 8;   // packed bytes of one row per stage
   static constexpr int RAW_BYTES = (MODE == kGemmDenseF32) ? 0 : BM * RAW_ROW;
   static constexpr int STAGE = A_BYTES + B_BYTES + RAW_BYTES;
   static constexpr int STAGES = (kSmemBudget / STAGE) > 8 ? 8 : (kSmemBudget / STAGE);
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;   // one fp32 accumulator
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;          // double-buffered
+  // double-buffered accumulators (the epilogue of a tile overlaps the next
+  // tile's MMAs); with A in tensor memory the A ring follows them:
+  // 2 x 192 + 2 stages x 64 columns
+  static constexpr int ACC_BUFS = 2;
+  static constexpr int TMEM_COLS = ATM ? 512 : 2 * ACC_COLS;
+  static constexpr int A_COL0 = ACC_BUFS * ACC_COLS;      // A ring (ATM): first column
+  static constexpr int A_COLS = BK * SK / 2;              // columns of one stage of A
+  static constexpr int A_STAGES = ATM ? (512 - A_COL0) / A_COLS : 1;
+  static_assert(!ATM || A_STAGES == 2, "A ring: one stage per dequantization team");
+  // dequantization warps: 8 cover a k-block (4 lane quarters x 2 halves of
+  // its 64 channels); with A in tensor memory two such teams take alternate
+  // stages (each its own stage of the A ring), so that one team dequantizes
+  // while the MMA consumes the other team's stage
+  static constexpr int DEQ_TEAMS = ATM ? 2 : 1;
+  static constexpr int DEQ_WARPS = 8 * DEQ_TEAMS;
+  static constexpr int THREADS = 64 + 32 * (DEQ_WARPS + kEpiWarps);
   static constexpr int SMEM = STAGES * STAGE + 1024 + 512;
 };
 
@@ -76,14 +102,18 @@ struct Abort {
   }
 };
 
-// bounded wait that also gives up as soon as another role has aborted
+// Bounded wait that also gives up as soon as another role has aborted.  The
+// waiting thread sleeps in the barrier (suspend hint) rather than polling:
+// the tensor-memory lane quarter of a warp is also its scheduler, so each
+// scheduler runs two dequantization warps beside an epilogue warp and (on two
+// of them) the producer or the MMA thread, and a polling waiter would take
+// issue slots from the dequantization it is waiting for.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const Abort& ab,
                                               unsigned bit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (ab.raised()) return false;
     if (globaltimer_ns() - t0 > wait_limit_ns()) {
       ab.raise(bit);
@@ -168,7 +198,7 @@ __device__ __forceinline__ uint4 dequant_word8(uint32_t w0, uint32_t w1, uint32_
 constexpr int kSzAhead = 4;
 
 template <int BN, int MODE, bool PERM, int BITS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, MODE, BITS>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_a,
                 const __half* __restrict__ scales, const uint32_t* __restrict__ zeros, int M,
                 int N, int K, int gs, void* __restrict__ out, int ldo,
@@ -189,7 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + S;     // [2]
   uint64_t* acc_empty = acc_full + 2; // [2]
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* a_full = drain + 1;             // [A_STAGES] (ATM)
+  uint64_t* a_empty = a_full + C::A_STAGES; // [A_STAGES] (ATM)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_empty + C::A_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const Abort ab{abort_flag};
 
@@ -224,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(deq + s, 32 * kDeqWarps);
+      mbar_init(deq + s, 32 * 8);
       mbar_init(empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -232,6 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acc_empty + b, 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
+    if (C::ATM)
+      for (int a = 0; a < C::A_STAGES; ++a) {
+        mbar_init(a_full + a, 32 * 8);
+        mbar_init(a_empty + a, 1);
+      }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
@@ -252,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // (warp-converged like the MMA issuer; one elected lane issues the copies)
+    {
       int it = 0;   // k-blocks issued by this CTA over all its tiles
       bool ok = true;
       // test hook: the first stage of the first CTA is never requested
@@ -261,26 +299,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tile, kb0, kb1, split;
         item_of(t, tile, kb0, kb1, split);
         const int n0 = (tile % n_tiles) * BM, m0 = (tile / n_tiles) * BN;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; kb += C::SK, ++it) {
           const int s = it % S;
-          if (it >= S && !wait_or_abort(empty + s, ((it / S) - 1) & 1, ab, 1u)) {
+          if (it >= S &&
+              !__all_sync(0xffffffffu, wait_or_abort(empty + s, ((it / S) - 1) & 1, ab, 1u))) {
             ok = false;
             break;
           }
           if (it == 0 && withhold) continue;
-          mbar_arrive_expect_tx(full + s, (MODE == kGemmDenseF32 ? C::A_BYTES : C::RAW_BYTES) +
-                                              C::B_BYTES);
-          if (MODE == kGemmDenseF32)
-            tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
-          else if (MODE == kGemmSiluF16) {
-            // 64 gate rows and the 64 matching up rows of the tile's pairs
-            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * KWB, n0 / 2);
-            tma_load_2d(sRaw + s * C::RAW_BYTES + (BM / 2) * C::RAW_ROW, &tm_a, full + s,
-                        kb * KWB, N / 2 + n0 / 2);
-          } else {
-            tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * KWB, n0);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(full + s, (MODE == kGemmDenseF32 ? C::A_BYTES : C::RAW_BYTES) +
+                                                C::B_BYTES);
+            if (MODE == kGemmDenseF32)
+              tma_load_2d(sA + s * C::A_BYTES, &tm_a, full + s, kb * BK, n0);
+            else if (MODE == kGemmSiluF16) {
+              // 64 gate rows and the 64 matching up rows of the tile's pairs
+              tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * KWB, n0 / 2);
+              tma_load_2d(sRaw + s * C::RAW_BYTES + (BM / 2) * C::RAW_ROW, &tm_a, full + s,
+                          kb * KWB, N / 2 + n0 / 2);
+            } else {
+              tma_load_2d(sRaw + s * C::RAW_BYTES, &tm_a, full + s, kb * KWB, n0);
+            }
+#pragma unroll
+            for (int j = 0; j < C::SK; ++j)
+              tma_load_2d(sB + s * C::B_BYTES + j * C::B_SUB, &tm_b, full + s, (kb + j) * BK, m0);
           }
-          tma_load_2d(sB + s * C::B_BYTES, &tm_b, full + s, kb * BK, m0);
+          __syncwarp();
         }
       }
       // the copies still in flight complete before the CTA may exit
@@ -289,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(full + s, (j / S) & 1))
           if (globaltimer_ns() - t0 > wait_limit_ns()) {
-            ab.raise(16u);
+            if (lane == 0) ab.raise(16u);
             break;
           }
       }
@@ -297,50 +341,207 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (its waits and descriptors warp-uniform)
+    // and one elected lane issues: measured on B300, a tcgen05.mma issued
+    // from a lone divergent thread costs about 96 cycles of issue, about 46
+    // (A in tensor memory) to 70 from a converged warp, and a 128 x 192 x 16
+    // MMA runs 96 cycles.  With A in tensor memory, a_full implies that the
+    // stage's activations have landed (the dequantization warps saw `full`
+    // before they arrived), so the MMA waits on a_full alone.
+    {
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
       int it = 0, lt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < items && ok; t += gridDim.x, ++lt) {
-        const int b = lt & 1;
-        if (lt >= 2 && !wait_or_abort(acc_empty + b, ((lt >> 1) - 1) & 1, ab, 2u)) break;
+        const int b = lt % C::ACC_BUFS;
+        if (lt >= C::ACC_BUFS &&
+            !__all_sync(0xffffffffu, wait_or_abort(acc_empty + b, ((lt / C::ACC_BUFS) - 1) & 1,
+                                                   ab, 2u)))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * C::ACC_COLS;
         int tile, kb0, kb1, split;
         item_of(t, tile, kb0, kb1, split);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; kb += C::SK, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!wait_or_abort(full + s, ph, ab, 2u) ||
-              (MODE != kGemmDenseF32 && !wait_or_abort(deq + s, ph, ab, 2u))) {
+          const int as = it % C::A_STAGES;
+          bool got;
+          if constexpr (C::ATM) {
+            got = wait_or_abort(a_full + as, (it / C::A_STAGES) & 1, ab, 2u);
+          } else {
+            got = wait_or_abort(full + s, ph, ab, 2u);
+            if (got && MODE != kGemmDenseF32) got = wait_or_abort(deq + s, ph, ab, 2u);
+          }
+          if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * C::A_BYTES));
           const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + s * C::B_BYTES));
+          if constexpr (C::ATM) {
+            const uint32_t at = tmem + C::A_COL0 + as * C::A_COLS;
+            if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-          umma_commit(empty + s);
+              for (int kk = 0; kk < C::SK * BK / 16; ++kk)
+                umma_f16_ts(d_tmem, at + kk * 8, bd + (kk >> 2) * (C::B_SUB >> 4) + 2 * (kk & 3),
+                            idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+              umma_commit(empty + s);
+              umma_commit(a_empty + as);
+            }
+          } else {
+            const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + s * C::A_BYTES));
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                umma_f16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc,
+                         (kb != kb0 || kk != 0) ? 1u : 0u);
+              umma_commit(empty + s);
+            }
+          }
+          __syncwarp();
         }
-        if (ok) umma_commit(acc_full + b);
+        if (ok && elect_one()) umma_commit(acc_full + b);
+        __syncwarp();
       }
-      umma_commit(drain);
+      if (elect_one()) umma_commit(drain);
+      __syncwarp();
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0))
         if (globaltimer_ns() - t0 > wait_limit_ns()) {
-          ab.raise(32u);
+          if (lane == 0) ab.raise(32u);
           break;
         }
     }
     __syncwarp();
-  } else if (warp < 2 + kDeqWarps) {
+  } else if (warp < 2 + C::DEQ_WARPS) {
     // ------------------------------------------------------------ dequant
-    if (MODE != kGemmDenseF32) {
-      const int d = warp - 2;              // 0..7
-      const int r = (d & 3) * 32 + lane;   // tile row
-      const int half = d >> 2;             // input channels 32*half .. +31 of the stage
+    if constexpr (C::ATM) {
+      // Team `team` (8 warps) dequantizes the stages (two k-blocks each)
+      // whose CTA-wide ordinal has parity `team`; a thread covers 32 channels
+      // (`half`) of each k-block for one row of its warp's tensor-memory lane
+      // quarter.
+      const int d = warp - 2;                 // 0..15
+      const int team = d >> 3;
+      const int half = (d >> 2) & 1;
+      const int r = (warp & 3) * 32 + lane;   // tile row = tensor-memory lane
+      constexpr int PW = 32 / BITS;           // codes per packed word
+      constexpr uint32_t QMASK = (1u << BITS) - 1u;
+      const int G = K / gs, ZW = (G + PW - 1) / PW;
+      const int gshift = gs == 128 ? 7 : gs == 64 ? 6 : 5;
+      // steps and zero points 8 groups at a time when rows hold whole blocks
+      // of 8 groups, the block after the current one loaded ahead
+      const bool blocks8 = (G % 8) == 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < items && ok; t += gridDim.x) {
+        int tile, kb0, kb1, split;
+        item_of(t, tile, kb0, kb1, split);
+        // with the fused gate/up weight, MMA row r of the tile is virtual row
+        // v = n0 + r: gate row v/2 for even v, up row v/2 for odd v
+        const int v = (tile % n_tiles) * BM + r;
+        const int n = MODE == kGemmSiluF16 ? (v >> 1) + (v & 1) * (N / 2) : v;
+        const bool row_ok = MODE == kGemmSiluF16 ? (v >> 1) < N / 2 : v < N;
+        const int raw_r = MODE == kGemmSiluF16 ? (r >> 1) + (r & 1) * (BM / 2) : r;
+        const __half* srow = scales + static_cast<size_t>(row_ok ? n : 0) * G;
+        const uint32_t* zrow = zeros + static_cast<size_t>(row_ok ? n : 0) * ZW;
+        uint4 sb0 = make_uint4(0, 0, 0, 0), sb1 = sb0;
+        uint32_t z00 = 0, z01 = 0, z10 = 0, z11 = 0;
+        auto load_blk = [&](int b, uint4& sb, uint32_t& za, uint32_t& zb) {
+          if (row_ok && 8 * b < G) {
+            sb = __ldg(reinterpret_cast<const uint4*>(srow + 8 * b));
+            za = __ldg(zrow + (8 * b) / PW);
+            zb = PW == 4 ? __ldg(zrow + (8 * b) / PW + 1) : 0u;
+          } else {
+            sb = make_uint4(0, 0, 0, 0);
+            za = zb = 0u;
+          }
+        };
+        int blk = -2, cur_g = -1;
+        uint32_t zbe = 0x64006400u, zbo = 0x54005400u;
+        __half2 s2 = __half2half2(__ushort_as_half(0));
+        // step and zero point of group gi (groups only move forward)
+        auto set_group = [&](int gi) {
+          if (gi == cur_g) return;
+          cur_g = gi;
+          uint32_t zc;
+          if (blocks8) {
+            const int b = gi >> 3;
+            if (b != blk) {
+              if (b == blk + 1) {
+                sb0 = sb1;
+                z00 = z10;
+                z01 = z11;
+              } else {
+                load_blk(b, sb0, z00, z01);
+              }
+              load_blk(b + 1, sb1, z10, z11);
+              blk = b;
+            }
+            const int j = gi & 7;
+            const uint32_t sw = (j >> 1) == 0 ? sb0.x : (j >> 1) == 1 ? sb0.y
+                              : (j >> 1) == 2 ? sb0.z : sb0.w;
+            s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(sw >> (16 * (j & 1)))));
+            zc = PW == 8 ? (z00 >> (4 * j)) & QMASK
+                         : (((j >> 2) == 0 ? z00 : z01) >> (8 * (j & 3))) & QMASK;
+          } else {
+            s2 = __half2half2(row_ok ? srow[gi] : __ushort_as_half(0));
+            zc = row_ok ? (__ldg(zrow + gi / PW) >> ((gi % PW) * BITS)) & QMASK : 0u;
+          }
+          zbe = (0x6400u | zc) * 0x00010001u;          // (1024 + z, 1024 + z)
+          zbo = (0x5400u | (zc << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
+        };
+        for (int kb = kb0; kb < kb1; kb += C::SK, ++it) {
+          if ((it & 1) != team) continue;
+          const int s = it % S;
+          const int as = it % C::A_STAGES;
+          // the warp stays converged for the tensor-memory stores
+          bool got = wait_or_abort(full + s, (it / S) & 1, ab, 4u);
+          if (got && it >= C::A_STAGES)
+            got = wait_or_abort(a_empty + as, ((it / C::A_STAGES) - 1) & 1, ab, 4u);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ta = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::A_COL0 +
+                              as * C::A_COLS + half * 16;
+#pragma unroll
+          for (int kl = 0; kl < C::SK; ++kl) {
+            set_group(((kb + kl) * BK + half * 32) >> gshift);
+            // this thread's 32 channels of k-block kb + kl
+            const uint8_t* rp = sRaw + s * C::RAW_BYTES + raw_r * C::RAW_ROW +
+                                kl * (C::RAW_ROW / C::SK) + half * (C::RAW_ROW / (2 * C::SK));
+            uint32_t cols[16];
+            if constexpr (BITS == 4) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(rp);
+              const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 o = dequant_word<PERM>(rw[i], zbe, zbo, s2);
+                cols[4 * i] = o.x; cols[4 * i + 1] = o.y; cols[4 * i + 2] = o.z; cols[4 * i + 3] = o.w;
+              }
+            } else {
+              const uint4 r0 = *reinterpret_cast<const uint4*>(rp);
+              const uint4 r1 = *reinterpret_cast<const uint4*>(rp + 16);
+              const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 o = dequant_word8<PERM>(rw[2 * i], rw[2 * i + 1], zbe, s2);
+                cols[4 * i] = o.x; cols[4 * i + 1] = o.y; cols[4 * i + 2] = o.z; cols[4 * i + 3] = o.w;
+              }
+            }
+            tmem_st16(ta + kl * (BK / 2), cols);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(a_full + as);
+        }
+      }
+    } else if (MODE != kGemmDenseF32) {
+      const int d = warp - 2;                 // 0..7
+      const int r = (warp & 3) * 32 + lane;   // tile row (= the warp's tensor-memory lanes)
+      const int half = d >> 2;                // input channels 32*half .. +31 of the stage
       constexpr int PW = 32 / BITS;        // codes per packed word
       constexpr uint32_t QMASK = (1u << BITS) - 1u;
       const int G = K / gs, ZW = (G + PW - 1) / PW;
@@ -478,9 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* pout = split >= 0 ? part + (static_cast<size_t>(tile - full_tiles) * ts + split) *
                                             BN * BM
                                : nullptr;
-      const int b = lt & 1;
+      const int b = lt % C::ACC_BUFS;
       const int n = n0 + quarter * 32 + lane;
-      if (!wait_or_abort(acc_full + b, (lt >> 1) & 1, ab, 8u)) break;
+      if (!wait_or_abort(acc_full + b, (lt / C::ACC_BUFS) & 1, ab, 8u)) break;
       tc_fence_after();
       float sq = 0.f;
       for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -659,7 +860,7 @@ int launch_tile(const CUtensorMap& tb, const CUtensorMap& ta, const __half* scal
   const int tiles = n_tiles * ((M + BN - 1) / BN);
   const int items = full_tiles + (tiles - full_tiles) * ts;
   cfg.gridDim = dim3(items < sms ? items : sms, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -693,6 +894,9 @@ int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __ha
     case 128:
       return launch_tile<128, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
                                                 yref, ldy, st, full_tiles, ts, kps, part);
+    case 192:
+      return launch_tile<192, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
+                                                yref, ldy, st, full_tiles, ts, kps, part);
     default:
       return launch_tile<256, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
                                                 yref, ldy, st, full_tiles, ts, kps, part);
@@ -705,7 +909,7 @@ int pick_bn(int M, int mode) {
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
-  return 256;
+  return 192;
 }
 
 }  // namespace
@@ -885,9 +1089,12 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
     rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Wd, K, N,
                       static_cast<uint64_t>(K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    const int pw = 32 / w_bit;   // codes per packed word
+    const int pw = 32 / w_bit;       // codes per packed word
+    // k-blocks per pipeline stage (Cfg::SK: 2 for the 192-token tile, whose
+    // A operand is in tensor memory)
+    const int sk = bn == 192 ? 2 : 1;
     rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, K / pw, N,
-                      static_cast<uint64_t>(K / pw) * 4, BK / pw,
+                      static_cast<uint64_t>(K / pw) * 4, sk * BK / pw,
                       mode == kGemmSiluF16 ? BM / 2 : BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (rc != AWQ_OK) return rc;
