@@ -259,53 +259,79 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
   // (8 channels k = 128 gl + 32 cc + 8 jj + i) sits at gl * 256 + jj * 64 +
   // cc * 16 and holds the pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) that the
   // dequantization produces
-  // Up to kBatch vectors per thread have their loads in flight together
-  // (the loads wait behind the weight stream in L2: one latency per batch)
-  const int nv = klen / 8, nitems = M * nv;
-  constexpr int kBatch = 4;
-  for (int base = threadIdx.x; base < nitems; base += kThreads * kBatch) {
-    uint4 xr[kBatch];
-    float4 ia[kBatch], ib[kBatch];
+  const int nv = klen / 8;
+  // x~ of token m, 8-channel vector v (inv_s given as is[], 1 when absent)
+  auto put = [&](int m, int v, const uint4& xr, const float (&is)[8]) {
+    const __half2* xh = reinterpret_cast<const __half2*>(&xr);
+    float f[8];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int q = base + u * kThreads;
-      if (q < nitems) {
-        const int m = q / nv, v = q - m * nv;
-        const int k = kbeg + 8 * v;
-        xr[u] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + k));
-        if (inv_s) {
-          ia[u] = __ldg(reinterpret_cast<const float4*>(inv_s + k));
-          ib[u] = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
+    for (int i = 0; i < 4; ++i) {
+      const float2 t2 = __half22float2(xh[i]);
+      f[2 * i] = __fmul_rn(t2.x, is[2 * i]);
+      f[2 * i + 1] = __fmul_rn(t2.y, is[2 * i + 1]);
+    }
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 p2 = __halves2half2(__float2half_rn(f[i]), __float2half_rn(f[i + 4]));
+      ow[i] = *reinterpret_cast<const uint32_t*>(&p2);
+    }
+    const int gl = v >> 4, cc = (v >> 2) & 3, jj = v & 3;
+    *reinterpret_cast<uint4*>(xsb + m * xstride + gl * 256 + jj * 64 + cc * 16) = o;
+  };
+  auto load_is = [&](int k, float (&is)[8]) {
+    if (inv_s) {
+      const float4 ia = __ldg(reinterpret_cast<const float4*>(inv_s + k));
+      const float4 ib = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
+      is[0] = ia.x; is[1] = ia.y; is[2] = ia.z; is[3] = ia.w;
+      is[4] = ib.x; is[5] = ib.y; is[6] = ib.z; is[7] = ib.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) is[i] = 1.f;
+    }
+  };
+  if (M <= 2) {
+    // Up to kBatch (token, vector) items per thread have their loads in
+    // flight together (the loads wait behind the weight stream in L2: one
+    // latency per batch)
+    const int nitems = M * nv;
+    constexpr int kBatch = 4;
+    for (int base = threadIdx.x; base < nitems; base += kThreads * kBatch) {
+      uint4 xr[kBatch];
+      float is[kBatch][8];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int q = base + u * kThreads;
+        if (q < nitems) {
+          const int m = q / nv, v = q - m * nv;
+          const int k = kbeg + 8 * v;
+          xr[u] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + k));
+          load_is(k, is[u]);
         }
       }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int q = base + u * kThreads;
+        if (q >= nitems) break;
+        const int m = q / nv;
+        put(m, q - m * nv, xr[u], is[u]);
+      }
     }
+  } else {
+    // one vector of every token per thread and round: inv_s read once per
+    // vector, all M loads in flight together
+    for (int v = threadIdx.x; v < nv; v += kThreads) {
+      const int k = kbeg + 8 * v;
+      float is[8];
+      load_is(k, is);
+      uint4 xr[8];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int q = base + u * kThreads;
-      if (q >= nitems) break;
-      const int m = q / nv, v = q - m * nv;
-      const __half2* xh = reinterpret_cast<const __half2*>(&xr[u]);
-      float f[8];
+      for (int m = 0; m < 8; ++m)
+        if (m < M) xr[m] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + k));
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 t2 = __half22float2(xh[i]);
-        f[2 * i] = t2.x;
-        f[2 * i + 1] = t2.y;
-      }
-      if (inv_s) {
-        const float is[8] = {ia[u].x, ia[u].y, ia[u].z, ia[u].w, ib[u].x, ib[u].y, ib[u].z, ib[u].w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], is[i]);
-      }
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 p2 = __halves2half2(__float2half_rn(f[i]), __float2half_rn(f[i + 4]));
-        ow[i] = *reinterpret_cast<const uint32_t*>(&p2);
-      }
-      const int gl = v >> 4, cc = (v >> 2) & 3, jj = v & 3;
-      *reinterpret_cast<uint4*>(xsb + m * xstride + gl * 256 + jj * 64 + cc * 16) = o;
+      for (int m = 0; m < 8; ++m)
+        if (m < M) put(m, v, xr[m], is);
     }
   }
   __syncthreads();
