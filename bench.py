@@ -47,8 +47,8 @@ METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofl
 # kernel source is byte-identical to the one that was captured.
 GEMV_TRAFFIC = {
     "source": "weight_only_bit_05_b300/csrc/awq_gemv_mma.cu",
-    "sha256": "6b4b21fd0ee7f3399476ca3281bdc3b0a6c284b2f6c90cfbb0b3bfffc52abd31",
-    "per_launch": {"qkv": 26229504, "o": 8796672, "gate_up": 46940928, "down": 23550720},
+    "sha256": "cfd05a1d73b5133f6d4ed774135bf41631480de896baa426c28266650c33bda2",
+    "per_launch": {"qkv": 26234880, "o": 8801024, "gate_up": 46935808, "down": 23555584},
 }
 
 
