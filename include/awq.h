@@ -181,7 +181,8 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
 /* ------------------------------------------------------------- GEMM, any M
  * Same result as awq_gemv for any M >= 1. For M <= 8 with the default format
  * (K % 256 == 0) it runs awq_gemv's decode matmul whenever that needs no K
- * split (the workspace is then unused). Otherwise on the 5th-generation
+ * split or halves K over a cluster of two (the workspace is then unused).
+ * Otherwise on the 5th-generation
  * tensor cores:
  * packed codes and activations staged by TMA, codes dequantized to fp16 in
  * shared memory, tcgen05.mma (fp16 x fp16, fp32 accumulation in tensor

@@ -418,11 +418,12 @@ int gemm_common(int mode, const awq_config* cfg, const uint16_t* X, int32_t M,
     return AWQ_ERR_WORKSPACE;
   }
   // up to 8 tokens of the default format: the decode matmul (warp-level MMA,
-  // weights streamed by TMA) when it runs without a K split; it scales the
-  // activations itself, so the workspace is not used
+  // weights streamed by TMA) when it runs without a K split or with K halved
+  // over a cluster of two; it scales the activations itself, so the
+  // workspace is not used
   if (mode == kGemmOutF16 && gemv_mma_eligible(M, K, c.w_bit, c.group, false)) {
     const MmaGemvPlan p = plan_gemv_mma(M, N, K, sm_count());
-    if (p.depth > 0 && p.nsplit == 1)
+    if (p.depth > 0 && p.nsplit <= 2)
       return launch_gemv_mma_plan(p, reinterpret_cast<const __half*>(X), M, qweight,
                                   reinterpret_cast<const __half*>(scales), zeros, inv_s, N, K,
                                   reinterpret_cast<__half*>(Y), st);
