@@ -8,20 +8,29 @@
 //                                               MMA N = BN tokens, K = 16/step)
 //
 // The kernel is persistent: one CTA per SM walks the (128 output channels x
-// BN tokens) tiles of Y^T, with warp roles
-//   warp 0      TMA producer: packed codes [128 rows x 8 words] and the
-//               activation tile [BN x 64] (128-byte swizzle) into an
-//               S-stage ring, completion counted on full[s];
-//   warp 1      allocates tensor memory (two accumulators) and issues
-//               tcgen05.mma (one thread), releasing stage s through
-//               tcgen05.commit -> empty[s] and a finished accumulator through
-//               tcgen05.commit -> acc_full[b];
-//   warps 2..9  dequantize each stage's codes (w^ = (q - z) * s in half2,
-//               written to the 128-byte-swizzled K-major operand layout),
-//               fence the async proxy and arrive on deq[s];
-//   warps 10-13 epilogue: read a finished accumulator from tensor memory
-//               (tcgen05.ld), write the outputs and free it (acc_empty[b]),
-//               while the next tile accumulates into the other buffer.
+// BN tokens) tiles of Y^T with warp roles.  Above 128 tokens (BN = 192) the
+// dequantized operand lives in tensor memory:
+//   warp 0       TMA producer (warp-converged, one elected lane): packed codes
+//                [128 rows x 16 words] and the activation tile as two [192 x
+//                64] boxes (128-byte swizzle) per 128-channel stage, into a
+//                4-stage ring, completion counted on full[s];
+//   warp 1       allocates tensor memory (two 192-column accumulators and two
+//                64-column operand stages) and issues tcgen05.mma with A from
+//                tensor memory, 8 per stage (warp-converged, one elected
+//                lane), releasing the stage through tcgen05.commit -> empty[s],
+//                the operand stage -> a_empty[a] and a finished accumulator
+//                -> acc_full[b];
+//   warps 2..17  two teams of 8 taking alternate stages: each thread turns 32
+//                channels of one row per k-block into w^ = (q - z) * s (half2)
+//                and writes them into its warp's lane quarter of the team's
+//                operand stage (tcgen05.st), then arrives on a_full[a];
+//   warps 18-21  epilogue: read a finished accumulator from tensor memory
+//                (tcgen05.ld), write the outputs and free it (acc_empty[b]),
+//                while the next tile accumulates into the other buffer.
+// At BN <= 128 and for the squared-error and dense passes of the scale
+// search (BN = 256) the operand goes through shared memory instead: 64-channel
+// stages, 8 dequantization warps writing the 128-byte-swizzled K-major layout
+// (deq[s]), both MMA operands read from shared memory, 4 epilogue warps.
 // Putting the weights on the MMA's M side means every CTA dequantizes its
 // 128 x K weight tile exactly once per BN tokens, and small token counts
 // (BN = 16) waste no tensor-core work on padding.  Consecutive tiles of the
