@@ -91,7 +91,8 @@ struct Cfg {
   static constexpr int A_COL0 = ACC_BUFS * ACC_COLS;      // A ring (ATM): first column
   static constexpr int A_COLS = BK * SK / 2;              // columns of one stage of A
   static constexpr int A_STAGES = ATM ? (512 - A_COL0) / A_COLS : 1;
-  static_assert(!ATM || A_STAGES == 2, "A ring: one stage per dequantization team");
+  static_assert(!ATM || (A_STAGES >= 2 && A_STAGES % 2 == 0),
+                "A ring: the same number of stages per dequantization team");
   // dequantization warps: 8 cover a k-block (4 lane quarters x 2 halves of
   // its 64 channels); with A in tensor memory two such teams take alternate
   // stages (each its own stage of the A ring), so that one team dequantizes
