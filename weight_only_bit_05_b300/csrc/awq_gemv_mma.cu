@@ -564,9 +564,12 @@ MmaGemvPlan make_gemv_mma_plan(int M, int N, int K, int sms, int warps, int ctas
 MmaGemvPlan plan_gemv_mma(int M, int N, int K, int sms) {
   MmaGemvPlan p = make_gemv_mma_plan(M, N, K, sms, 8, 2, 2, 2);
   if (p.depth > 0 && p.nsplit == 1) return p;
-  // one 16-warp CTA per SM: the whole K, else K halved over a cluster of two
+  // one 16-warp CTA per SM: the whole K, else K halved over a cluster of two,
+  // with 2-deep rings, else with 1-deep ones (16 stages in flight per SM)
   const MmaGemvPlan q = make_gemv_mma_plan(M, N, K, sms, 16, 1, 2, 2);
   if (q.depth > 0 && q.nsplit <= 2) return q;
+  const MmaGemvPlan q1 = make_gemv_mma_plan(M, N, K, sms, 16, 1, 1, 1);
+  if (q1.depth > 0 && q1.nsplit <= 2) return q1;
   if (p.depth == 0) p = make_gemv_mma_plan(M, N, K, sms, 8, 1, 2, kMaxDepth);
   return p;
 }
