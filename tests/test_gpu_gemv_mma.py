@@ -140,3 +140,20 @@ def test_gemv_right_after_pack():
         rq, rs, rz = O.awq_pack(W, None)
         assert np.array_equal(host(qw), rq)
         assert_linear_close(y, X, rq, rs, rz, None)
+
+
+# plans on 148 SMs: 16 warps with K halved over a cluster of two and 1-deep
+# rings (8, 520, 11008), (7, 264, 16384); 2-deep rings (8, 1096, 8192),
+# (3, 136, 28672); 16 warps without a split (5, 264, 8192)
+@pytest.mark.parametrize("M,N,K", [(8, 520, 11008), (7, 264, 16384), (8, 1096, 8192),
+                                   (3, 136, 28672), (5, 264, 8192)])
+def test_gemm_routes_cluster_plans(M, N, K):
+    """awq_gemm at up to 8 tokens runs the decode matmul also when it halves K
+    over a cluster of two (with 2- or 1-deep rings): per element against the
+    oracle, and the same bits as awq_gemv for the same call."""
+    qw, sc, zs, inv_s = _layer(N, K, 77 + M)
+    X = _tokens(M, K, 80 + M)
+    args = (dev(X), dev(qw), dev(sc), dev(zs), dev(inv_s))
+    y = awq.gemm(*args)
+    assert torch.equal(y, awq.gemv(*args))
+    assert_linear_close(host(y), X, qw, sc, zs, inv_s)
