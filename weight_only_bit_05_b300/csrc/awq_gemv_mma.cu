@@ -7,15 +7,15 @@
 //
 //  * Weights first.  A CTA owns a balanced range of output rows (and, when
 //    the activations of the whole K do not fit in shared memory, a K slice of
-//    a thread-block cluster).  Its eight warps split the range's stages of 16
+//    a thread-block cluster).  Its warps (8 or 16) split the range's stages of 16
 //    rows x 512 input channels (4 KB of codes as two 2 KB TMA boxes with the
 //    128-byte swizzle, plus the stage's steps and zero points by 4-byte
 //    cp.async) into contiguous runs, each warp streaming its run through its
 //    own ring of slots, so that a warp only ever waits on its own slots, in
 //    order.  Packed weights, steps and zero points never depend on the
 //    previous kernel in the stream, so each warp fills its ring BEFORE
-//    griddepcontrol.wait (programmatic dependent launch).  Two CTAs of a
-//    launch share an SM.
+//    griddepcontrol.wait (programmatic dependent launch).  At one token two
+//    8-warp CTAs of a launch share an SM.
 //  * Dot products on the warp-level tensor-core MMA (mma.sync m16n8k16, fp16
 //    operands, fp32 accumulation): the 16 weight rows of a stage are the A
 //    operand, the (up to 8) tokens the N side.  On CUDA cores the same
@@ -559,8 +559,9 @@ MmaGemvPlan make_gemv_mma_plan(int M, int N, int K, int sms, int warps, int ctas
 // ring of two 4 KB stages (fastest at M = 1, against deeper rings, one CTA of
 // 8, 12 or 16 warps per SM, and one CTA beside the next launch's); when the
 // activations of several tokens do not fit half an SM, one CTA of sixteen
-// warps per SM (the activations once per SM); a K split over a cluster only
-// when neither fits.
+// warps per SM (the activations once per SM), with K halved over a cluster of
+// two and then with 1-deep rings if needed (70B qkv and 7B down at 8 tokens);
+// wider K splits over a cluster only when none of these fits.
 MmaGemvPlan plan_gemv_mma(int M, int N, int K, int sms) {
   MmaGemvPlan p = make_gemv_mma_plan(M, N, K, sms, 8, 2, 2, 2);
   if (p.depth > 0 && p.nsplit == 1) return p;
