@@ -47,8 +47,8 @@ METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofl
 # kernel source is byte-identical to the one that was captured.
 GEMV_TRAFFIC = {
     "source": "weight_only_bit_05_b300/csrc/awq_gemv_mma.cu",
-    "sha256": "cfd05a1d73b5133f6d4ed774135bf41631480de896baa426c28266650c33bda2",
-    "per_launch": {"qkv": 26234880, "o": 8801024, "gate_up": 46935808, "down": 23555584},
+    "sha256": "8bfac337a2550773d5e378a35cac88dcdfd144bd7fcb96f8ec2feaf0d6906851",
+    "per_launch": {"qkv": 26233856, "o": 8800768, "gate_up": 46935296, "down": 23555328},
 }
 
 
