@@ -138,14 +138,17 @@ struct MmaLayout {
 
 // kWarps warps, each streaming its own contiguous run of stages through its
 // own ring (a warp waits only on its own slots, in order); MINB CTAs per SM
-// for the register budget.
-template <int kWarps, int MINB>
+// for the register budget; kDepth slots per ring (0: the run-time depth_rt),
+// a constant for the plans the library uses so that the slot and phase
+// arithmetic of every stage folds away.
+template <int kWarps, int MINB, int kDepth>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap tq, const __half* __restrict__ X,
                     const __half* __restrict__ scales, const uint32_t* __restrict__ zeros,
-                    const float* __restrict__ inv_s, int M, int N, int K, int KS, int depth,
+                    const float* __restrict__ inv_s, int M, int N, int K, int KS, int depth_rt,
                     int rows_cap, __half* __restrict__ Y) {
   constexpr int kThreads = kWarps * 32;
+  const int depth = kDepth > 0 ? kDepth : depth_rt;
   extern __shared__ uint8_t smem_raw[];
   // the 128-byte swizzle of the TMA boxes follows shared-memory address bits
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -580,11 +583,11 @@ bool gemv_mma_eligible(int M, int K, int w_bit, int group, bool silu_mul) {
 }
 
 namespace {
-template <int W, int MINB>
+template <int W, int MINB, int D>
 int launch_mma(const MmaGemvPlan& p, const CUtensorMap& tq, const __half* X, int M,
                const __half* scales, const uint32_t* zeros, const float* inv_s, int N, int K,
                __half* Y, cudaStream_t st) {
-  auto kern = gemv_mma_kernel<W, MINB>;
+  auto kern = gemv_mma_kernel<W, MINB, D>;
   const int rc = ensure_smem_attr(reinterpret_cast<const void*>(kern), p.smem);
   if (rc != AWQ_OK) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -619,12 +622,15 @@ int launch_gemv_mma_plan(const MmaGemvPlan& p, const __half* X, int M, const uin
                               static_cast<uint64_t>(K) / 8, static_cast<uint64_t>(N),
                               static_cast<uint64_t>(K) / 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != AWQ_OK) return rc;
-#define AWQ_MMA_CASE(W, B)                                                                     \
-  if (p.warps == W && p.ctas_per_sm == B)                                                      \
-    return launch_mma<W, B>(p, tq, X, M, scales, zeros, inv_s, N, K, Y, st);
-  AWQ_MMA_CASE(8, 2)
-  AWQ_MMA_CASE(8, 1)
-  AWQ_MMA_CASE(16, 1)
+#define AWQ_MMA_CASE(W, B, D)                                                                  \
+  if (p.warps == W && p.ctas_per_sm == B && (D == 0 || p.depth == D))                          \
+    return launch_mma<W, B, D>(p, tq, X, M, scales, zeros, inv_s, N, K, Y, st);
+  AWQ_MMA_CASE(8, 2, 2)
+  AWQ_MMA_CASE(16, 1, 2)
+  AWQ_MMA_CASE(16, 1, 1)
+  AWQ_MMA_CASE(8, 2, 0)
+  AWQ_MMA_CASE(8, 1, 0)
+  AWQ_MMA_CASE(16, 1, 0)
 #undef AWQ_MMA_CASE
   set_error("awq_gemv: no kernel for %d warps at %d CTAs per SM", p.warps, p.ctas_per_sm);
   return AWQ_ERR_UNSUPPORTED;
