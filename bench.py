@@ -47,8 +47,8 @@ METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofl
 # kernel source is byte-identical to the one that was captured.
 GEMV_TRAFFIC = {
     "source": "weight_only_bit_05_b300/csrc/awq_gemv_mma.cu",
-    "sha256": "8bfac337a2550773d5e378a35cac88dcdfd144bd7fcb96f8ec2feaf0d6906851",
-    "per_launch": {"qkv": 26233856, "o": 8800768, "gate_up": 46935296, "down": 23555328},
+    "sha256": "6f1064e4639c395b61d619e068370fd247647d3f21171a01746a0bd6b5071263",
+    "per_launch": {"qkv": 26230016, "o": 8796416, "gate_up": 46931456, "down": 23550976},
 }
 
 
