@@ -37,7 +37,7 @@ def test_default_config_and_workspace_sizes():
     # (up to 128 tokens) or of each [bn][128] tile (bn = the token tile) for
     # the wide one
     for M, N, K, bn in ((16, 256, 4096, 16), (120, 256, 4096, 128), (48, 640, 8192, 64),
-                        (300, 1024, 8192, 192)):
+                        (300, 1024, 8192, 160)):
         xt = ((M * K * 2 + 255) // 256) * 256
         part = lib.awq_gemm_workspace_size(M, N, K) - xt
         padded = -(-M // bn) * bn * -(-N // 128) * 128 * 4

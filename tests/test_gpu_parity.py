@@ -120,7 +120,7 @@ def test_gemv_parity(M, N, K):
     assert_linear_close(host(y0), X16, qw, sc, zs, None)
 
 
-@pytest.mark.parametrize("M", [1, 7, 16, 17, 33, 64, 100, 128, 129, 192, 193, 256, 300, 384, 513])
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 33, 64, 100, 128, 129, 160, 161, 192, 193, 256, 300, 320, 384, 513])
 @pytest.mark.parametrize("N,K", [(512, 512), (136, 384), (8, 128), (264, 1152)])
 def test_gemm_parity(M, N, K):
     rng, qw, sc, zs, inv_s = _packed(M * 7 + N * 3 + K, N, K)

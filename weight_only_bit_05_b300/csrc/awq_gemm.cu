@@ -8,23 +8,23 @@
 //                                               MMA N = BN tokens, K = 16/step)
 //
 // The kernel is persistent: one CTA per SM walks the (128 output channels x
-// BN tokens) tiles of Y^T with warp roles.  Above 128 tokens (BN = 192) the
+// BN tokens) tiles of Y^T with warp roles.  Above 128 tokens (BN = 160) the
 // dequantized operand lives in tensor memory:
 //   warp 0       TMA producer (warp-converged, one elected lane): packed codes
-//                [128 rows x 16 words] and the activation tile as two [192 x
+//                [128 rows x 16 words] and the activation tile as two [160 x
 //                64] boxes (128-byte swizzle) per 128-channel stage, into a
 //                4-stage ring, completion counted on full[s];
-//   warp 1       allocates tensor memory (two 192-column accumulators and two
+//   warp 1       allocates tensor memory (two 160-column accumulators and three
 //                64-column operand stages) and issues tcgen05.mma with A from
 //                tensor memory, 8 per stage (warp-converged, one elected
 //                lane), releasing the stage through tcgen05.commit -> empty[s],
 //                the operand stage -> a_empty[a] and a finished accumulator
 //                -> acc_full[b];
-//   warps 2..17  two teams of 8 taking alternate stages: each thread turns 32
+//   warps 2..25  three teams of 8 taking stages in turn: each thread turns 32
 //                channels of one row per k-block into w^ = (q - z) * s (half2)
 //                and writes them into its warp's lane quarter of the team's
 //                operand stage (tcgen05.st), then arrives on a_full[a];
-//   warps 18-21  epilogue: read a finished accumulator from tensor memory
+//   warps 26-29  epilogue: read a finished accumulator from tensor memory
 //                (tcgen05.ld), write the outputs and free it (acc_empty[b]),
 //                while the next tile accumulates into the other buffer.
 // At BN <= 128 and for the squared-error and dense passes of the scale
@@ -61,9 +61,9 @@ __device__ __forceinline__ uint64_t wait_limit_ns() {
 }
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
-// At BN = 192 the dequantized operand does not pass through shared memory:
+// At BN = 160 the dequantized operand does not pass through shared memory:
 // the dequantization warps write it into a ring in tensor memory (after the
-// two 192-column accumulators) and the MMA reads A from there.  Shared memory
+// two 160-column accumulators) and the MMA reads A from there.  Shared memory
 // then carries only the activation tile and the packed codes of a stage (and
 // the MMA reads only the activations from it), which keeps its port below
 // the rate at which the MMA consumes stages; with A in shared memory a
@@ -71,7 +71,7 @@ constexpr int kSmemBudget = 227 * 1024 - 2048;
 // in the 512 cycles of the stage's MMA.
 template <int BN, int MODE, int BITS>
 struct Cfg {
-  static constexpr bool ATM = BN == 192;
+  static constexpr bool ATM = BN == 160;
   // 64-channel k-blocks per pipeline stage: two with A in tensor memory, so
   // that every wait, commit and arrive of the roles serves 8 MMAs, not 4
   static constexpr int SK = ATM ? 2 : 1;
@@ -85,19 +85,19 @@ struct Cfg {
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;   // one fp32 accumulator
   // double-buffered accumulators (the epilogue of a tile overlaps the next
   // tile's MMAs); with A in tensor memory the A ring follows them:
-  // 2 x 192 + 2 stages x 64 columns
+  // 2 x 160 + 3 stages x 64 columns
   static constexpr int ACC_BUFS = 2;
   static constexpr int TMEM_COLS = ATM ? 512 : 2 * ACC_COLS;
   static constexpr int A_COL0 = ACC_BUFS * ACC_COLS;      // A ring (ATM): first column
   static constexpr int A_COLS = BK * SK / 2;              // columns of one stage of A
   static constexpr int A_STAGES = ATM ? (512 - A_COL0) / A_COLS : 1;
-  static_assert(!ATM || (A_STAGES >= 2 && A_STAGES % 2 == 0),
-                "A ring: the same number of stages per dequantization team");
   // dequantization warps: 8 cover a k-block (4 lane quarters x 2 halves of
-  // its 64 channels); with A in tensor memory two such teams take alternate
-  // stages (each its own stage of the A ring), so that one team dequantizes
-  // while the MMA consumes the other team's stage
-  static constexpr int DEQ_TEAMS = ATM ? 2 : 1;
+  // its 64 channels); with A in tensor memory three such teams take the
+  // stages in turn, each into its own stage of the A ring, so that two teams
+  // dequantize while the MMA consumes the third team's stage (a team's
+  // dequantization of a stage takes longer than the stage's MMAs)
+  static constexpr int DEQ_TEAMS = ATM ? 3 : 1;
+  static_assert(!ATM || A_STAGES == DEQ_TEAMS, "A ring: one stage per dequantization team");
   static constexpr int DEQ_WARPS = 8 * DEQ_TEAMS;
   static constexpr int THREADS = 64 + 32 * (DEQ_WARPS + kEpiWarps);
   static constexpr int SMEM = STAGES * STAGE + 1024 + 512;
@@ -354,8 +354,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, BITS>::THREADS, 1)
     // The whole warp runs the loop (its waits and descriptors warp-uniform)
     // and one elected lane issues: measured on B300, a tcgen05.mma issued
     // from a lone divergent thread costs about 96 cycles of issue, about 46
-    // (A in tensor memory) to 70 from a converged warp, and a 128 x 192 x 16
-    // MMA runs 96 cycles.  With A in tensor memory, a_full implies that the
+    // (A in tensor memory) to 70 from a converged warp, and a 128 x 160 x 16
+    // MMA runs 80 cycles.  With A in tensor memory, a_full implies that the
     // stage's activations have landed (the dequantization warps saw `full`
     // before they arrived), so the MMA waits on a_full alone.
     {
@@ -428,10 +428,10 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, BITS>::THREADS, 1)
     // ------------------------------------------------------------ dequant
     if constexpr (C::ATM) {
       // Team `team` (8 warps) dequantizes the stages (two k-blocks each)
-      // whose CTA-wide ordinal has parity `team`; a thread covers 32 channels
-      // (`half`) of each k-block for one row of its warp's tensor-memory lane
-      // quarter.
-      const int d = warp - 2;                 // 0..15
+      // whose CTA-wide ordinal is `team` modulo the number of teams; a thread
+      // covers 32 channels (`half`) of each k-block for one row of its warp's
+      // tensor-memory lane quarter.
+      const int d = warp - 2;                 // 0 .. DEQ_WARPS - 1
       const int team = d >> 3;
       const int half = (d >> 2) & 1;
       const int r = (warp & 3) * 32 + lane;   // tile row = tensor-memory lane
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, BITS>::THREADS, 1)
           zbo = (0x5400u | (zc << 4)) * 0x00010001u;   // (64 + z, 64 + z), 4-bit only
         };
         for (int kb = kb0; kb < kb1; kb += C::SK, ++it) {
-          if ((it & 1) != team) continue;
+          if (it % C::DEQ_TEAMS != team) continue;
           const int s = it % S;
           const int as = it % C::A_STAGES;
           // the warp stays converged for the tensor-memory stores
@@ -904,8 +904,8 @@ int dispatch_bn(int bn, const CUtensorMap& tb, const CUtensorMap& ta, const __ha
     case 128:
       return launch_tile<128, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
                                                 yref, ldy, st, full_tiles, ts, kps, part);
-    case 192:
-      return launch_tile<192, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
+    case 160:
+      return launch_tile<160, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
                                                 yref, ldy, st, full_tiles, ts, kps, part);
     default:
       return launch_tile<256, MODE, PERM, BITS>(tb, ta, scales, zeros, M, N, K, gs, out, ldo,
@@ -919,7 +919,7 @@ int pick_bn(int M, int mode) {
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
-  return 192;
+  return 160;
 }
 
 }  // namespace
@@ -1100,9 +1100,9 @@ int launch_gemm(int mode, const __half* Xt, bool xt_permuted, int M, const uint3
                       static_cast<uint64_t>(K) * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     const int pw = 32 / w_bit;       // codes per packed word
-    // k-blocks per pipeline stage (Cfg::SK: 2 for the 192-token tile, whose
+    // k-blocks per pipeline stage (Cfg::SK: 2 for the 160-token tile, whose
     // A operand is in tensor memory)
-    const int sk = bn == 192 ? 2 : 1;
+    const int sk = bn == 160 ? 2 : 1;
     rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, K / pw, N,
                       static_cast<uint64_t>(K / pw) * 4, sk * BK / pw,
                       mode == kGemmSiluF16 ? BM / 2 : BM, CU_TENSOR_MAP_SWIZZLE_NONE);
