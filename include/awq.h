@@ -184,9 +184,11 @@ AWQ_API int awq_gemv_ex(const awq_config* cfg, const uint16_t* X, int32_t M,
  * split or halves K over a cluster of two (the workspace is then unused).
  * Otherwise on the 5th-generation
  * tensor cores:
- * packed codes and activations staged by TMA, codes dequantized to fp16 in
- * shared memory, tcgen05.mma (fp16 x fp16, fp32 accumulation in tensor
- * memory). For M <= 128 with 4- or 8-bit codes in 128- or 64-channel groups
+ * packed codes and activations staged by TMA, codes dequantized to fp16
+ * (into tensor memory for the tcgen05.mma's A operand above 128 tokens,
+ * into shared memory otherwise), tcgen05.mma (fp16 x fp16, fp32
+ * accumulation in tensor memory). For M <= 128 with 4- or 8-bit codes in
+ * 128- or 64-channel groups
  * a narrow-token kernel runs instead: the operand holds the exact integers
  * q - z in tensor memory, each group's partial sum is accumulated on its own
  * and multiplied by the group step in fp32 (so it rounds differently from
