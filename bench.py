@@ -354,7 +354,7 @@ def gemm_prefill(awq, torch, pk, reps=5):
             "per_shape_tflops": out, "includes": "X~ = fp16(X*inv_s) prescale + tcgen05 GEMM"}
 
 
-def gemv_70b(awq, torch, hbm, reps=20):
+def gemv_70b(awq, torch, hbm, reps=200):
     """GB/s of awq_gemv at M = 1 on the four Llama-2-70B shapes: a CUDA graph
     of launches over enough packed-weight copies that they cannot stay in L2."""
     dev = torch.device("cuda")
