@@ -47,8 +47,8 @@ METRIC = "W4A16 GEMV GB/s & GEMM TFLOPS on Llama-2 shapes, % of HBM/tensor roofl
 # kernel source is byte-identical to the one that was captured.
 GEMV_TRAFFIC = {
     "source": "weight_only_bit_05_b300/csrc/awq_gemv_mma.cu",
-    "sha256": "6f1064e4639c395b61d619e068370fd247647d3f21171a01746a0bd6b5071263",
-    "per_launch": {"qkv": 26230016, "o": 8796416, "gate_up": 46931456, "down": 23550976},
+    "sha256": "650d3170b1f549c3c8c39f8f01c73d9f8cb37392388c3df94bd1e2675726a437",
+    "per_launch": {"qkv": 26229504, "o": 8796160, "gate_up": 46930688, "down": 23551232},
 }
 
 

@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
       const uint32_t zae = za * 0x00010001u + 0x64006400u, zao = za * 0x00100010u + 0x54005400u;
       const uint32_t zbe = zb * 0x00010001u + 0x64006400u, zbo = zb * 0x00100010u + 0x54005400u;
       const uint8_t* xg = xst + h * 256;
-      float d0[4], d1[4];
+      float d0[4];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const uint32_t wa = jj == 0 ? qa.x : jj == 1 ? qa.y : jj == 2 ? qa.z : qa.w;
@@ -419,18 +419,14 @@ __global__ void __launch_bounds__(kWarps * 32, MINB)
         const uint32_t b2 = hsub2_u(and_or(tb, 0x000F000Fu, 0x64006400u), zbe);
         const uint32_t b3 = hsub2_u(and_or(tb, 0x00F000F0u, 0x54005400u), zbo);
         // logical k (2c, 2c+1) <- (k0, k4), (2c+8, 2c+9) <- (k1, k5); and (k2, k6), (k3, k7)
-        if (jj == 0) {
-          mma16816_first(d0, a0, b0, a1, b1, xv.x, xv.y);
-          mma16816_first(d1, a2, b2, a3, b3, xv.z, xv.w);
-        } else {
-          mma16816(d0, a0, b0, a1, b1, xv.x, xv.y);
-          mma16816(d1, a2, b2, a3, b3, xv.z, xv.w);
-        }
+        if (jj == 0) mma16816_first(d0, a0, b0, a1, b1, xv.x, xv.y);
+        else mma16816(d0, a0, b0, a1, b1, xv.x, xv.y);
+        mma16816(d0, a2, b2, a3, b3, xv.z, xv.w);
       }
-      acc[0] = fmaf(s_a[h], d0[0] + d1[0], acc[0]);
-      acc[1] = fmaf(s_a[h], d0[1] + d1[1], acc[1]);
-      acc[2] = fmaf(s_b[h], d0[2] + d1[2], acc[2]);
-      acc[3] = fmaf(s_b[h], d0[3] + d1[3], acc[3]);
+      acc[0] = fmaf(s_a[h], d0[0], acc[0]);
+      acc[1] = fmaf(s_a[h], d0[1], acc[1]);
+      acc[2] = fmaf(s_b[h], d0[2], acc[2]);
+      acc[3] = fmaf(s_b[h], d0[3], acc[3]);
     };
     if (kbeg + klen - kc >= kStageK) {
 #pragma unroll
