@@ -43,6 +43,14 @@ def test_default_config_and_workspace_sizes():
         padded = -(-M // bn) * bn * -(-N // 128) * 128 * 4
         assert part > 0 and part % 4 == 0 and part <= 8 * max(padded, M * N * 4), (M, N, K)
     assert lib.awq_gemm_workspace_size(0, 512, 512) == 0
+    # Without a device the library plans for 148 SMs.  160-token tiles:
+    # 2048 x 3584 has 28 x 13 = 364 tiles, two full rounds and 68 left, so
+    # only those 68 tiles are split over K, 2 parts each (68 x 2 <= 148
+    # SMs), one [160][128] fp32 block per part; 160 x 18944 has exactly one
+    # round of 148 tiles and no split.
+    xt = 2048 * 4096 * 2
+    assert lib.awq_gemm_workspace_size(2048, 3584, 4096) == xt + 68 * 2 * 160 * 128 * 4
+    assert lib.awq_gemm_workspace_size(160, 18944, 4096) == 160 * 4096 * 2
     assert lib.awq_absmean_workspace_size(4096, 4096) % 8 == 0
     assert lib.awq_absmean_workspace_size(4096, 4096) >= 4096 * 8
     ws = lib.awq_search_workspace_size(65536, 57344, 8192)
